@@ -1,0 +1,96 @@
+"""Algorithmic byte and FLOP model of the GDN chunked-prefill forward.
+
+Bytes: every tensor that must cross HBM once and only once - q, k, v, o in the
+input dtype, g and beta in fp32 (one scalar per token and v head), and the
+fp32 [dk, dv] state per (sequence, v head) read (h0) and written (hT).  This is
+the "ideal resident" global-memory traffic of "Empowering Hybrid Attention
+Models on NPUs", Figure 4(a): at T=2048, H=10, d=128 with FP16 Q/K/V/O and
+FP32 gates and state it gives 21.41 MiB for GDN, and 31.33 MiB once the gate
+is per channel as in KDA (checked by a golden test).
+
+FLOPs: per token and v head, counting only the triangles the method needs
+(strictly lower KK^T, lower-with-diagonal QK^T and its product with V_new,
+lower-triangular Tm in the W/U products, the solve, and the three dk x dv
+state products: W h, Q h and the update), times 2.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+# sm_103a: 152 SMs, 128 fp32 lanes per SM, one FMA (2 FLOP) per lane per clock.
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+
+
+def load_peaks(path=None):
+    """Measured peaks (HBM GB/s, dense bf16 TFLOP/s); falls back to fixed figures.
+
+    Returns (peaks dict, source) with source "measured" or "fallback".
+    """
+    if path is None:
+        path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        if pk.get("hbm_gbs") and pk.get("bf16_tflops"):
+            return pk, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def io_bytes(T_total, n_seqs, Hqk, Hv, dk, dv, elem_bytes, h0_read=False, hT_written=True,
+             gate_per_channel=False):
+    """Bytes that must cross HBM once: q, k, v, o, g, beta, h0, hT."""
+    per_token = 2 * Hqk * dk * elem_bytes + 2 * Hv * dv * elem_bytes
+    per_token += Hv * 4 * (dk if gate_per_channel else 1)   # g
+    per_token += Hv * 4                                       # beta
+    state = n_seqs * Hv * dk * dv * 4
+    return T_total * per_token + state * (int(h0_read) + int(hT_written))
+
+
+def macs_per_token_head(chunk, dk, dv):
+    """Multiply-adds per token per v head (triangles only)."""
+    C = chunk
+    kkt = (C - 1) / 2 * dk
+    qkt = (C + 1) / 2 * dk
+    wu = (C + 1) / 2 * (dk + dv)
+    solve = C * C / 6
+    state = 3 * dk * dv
+    pv = (C + 1) / 2 * dv
+    return kkt + qkt + wu + solve + state + pv
+
+
+def flops(T_total, Hv, chunk, dk, dv):
+    return 2.0 * T_total * Hv * macs_per_token_head(chunk, dk, dv)
+
+
+def decode_bytes(n_seqs, Hqk, Hv, dk, dv, elem_bytes):
+    """One decode step: the fp32 state read and written, plus one token of q, k, v, o, g, beta."""
+    return (n_seqs * Hv * dk * dv * 4 * 2
+            + n_seqs * (2 * Hqk * dk + 2 * Hv * dv) * elem_bytes + n_seqs * Hv * 8)
+
+
+def fp32_alu_tflops(sm_mhz):
+    return SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def workload_model(w, peaks):
+    """Bytes, FLOPs and roofline time of one forward call of workload ``w``."""
+    eb = 4 if w.dtype == "f32" else 2
+    b = io_bytes(w.T_total, w.n_seqs, w.Hqk, w.Hv, w.dk, w.dv, eb,
+                 h0_read=w.h0_std is not None, hT_written=True)
+    f = flops(w.T_total, w.Hv, w.chunk, w.dk, w.dv)
+    t_hbm = b / (peaks["hbm_gbs"] * 1e9)
+    if w.dtype == "f32":
+        tc = fp32_alu_tflops(peaks.get("sm_max_mhz", 2070.0)) * 1e12
+    else:
+        tc = peaks["bf16_tflops"] * 1e12
+    t_fl = f / tc
+    return dict(bytes=b, flops=f, t_hbm=t_hbm, t_flop=t_fl, t_roof=max(t_hbm, t_fl),
+                bound="hbm" if t_hbm >= t_fl else ("alu" if w.dtype == "f32" else "tensor"))
