@@ -1,0 +1,362 @@
+"""Benchmark: GDN chunked-prefill tokens/s per layer on GB300, with roofline fraction.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+One step = one gdn_chunk_fwd call (every operator of the chunkwise forward)
+over one batch of the headline workload (16 heads of 128, 4096 tokens, bf16;
+see linear_attention_prefill_gb300/workloads.py).  Inputs are resident in HBM
+when timing starts; L2 (129 MB) is flushed by writing a 320 MB buffer before
+every timed step, outside the timed events.  Each step is timed with CUDA events
+on the launching stream; the job time is the max over ranks.  Under torchrun
+every rank runs its own batch (weak scaling, no collective on the data path).
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle legs time one core: keep BLAS from spawning threads
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_prefill_gb300 import roofline  # noqa: E402
+from linear_attention_prefill_gb300.sharding import rank_seed, reduce_timing  # noqa: E402
+from linear_attention_prefill_gb300.workloads import HEADLINE, WORKLOADS, make_decode_inputs, make_inputs  # noqa: E402
+
+METRIC = "GDN chunked-prefill tokens/s per layer on 1 GB300; % of TC/HBM roofline"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 320 * 2 ** 20
+KERNEL_NAME = "gdn_fwd_bf16_kernel"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "linear_attention_prefill_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this exact source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def config_of(w, world, extra=None):
+    cfg = {"workload": w.name, "seqlens": list(w.seqlens) if len(w.seqlens) <= 16 else len(w.seqlens),
+           "T_total": w.T_total, "Hqk": w.Hqk, "Hv": w.Hv, "dk": w.dk, "dv": w.dv,
+           "chunk": w.chunk, "h0": w.h0_std is not None, "global_batch": w.n_seqs * world,
+           "seq_len": max(w.seqlens), "l2": "flushed (320 MB write) before every timed step",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) >= 10]
+        self.file.close()
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        mhz = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        max_mhz = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(max_mhz) if max_mhz else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def run_decode(lap, w, dev, steps=200):
+    """µs per gdn_recurrent_step on this workload's state shape, plain and as a CUDA graph."""
+    N, Hv = w.n_seqs, w.Hv
+    h = torch.randn((N, Hv, w.dk, w.dv), device=dev) * 0.1
+    d = make_decode_inputs(w, 0, device=dev)
+    o = torch.empty((N, Hv, w.dv), dtype=d["q"].dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        lap.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], h, o)
+
+    for _ in range(10):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    plain = a.elapsed_time(b) * 1e3 / steps
+    graph_us = None
+    try:
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            one()
+        stream.wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(100):
+                one()
+        g.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps // 100):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_us = a.elapsed_time(b) * 1e3 / (100 * (steps // 100))
+    except RuntimeError:
+        graph_us = None
+    nbytes = roofline.decode_bytes(N, w.Hqk, Hv, w.dk, w.dv, 2 if w.dtype == "bf16" else 4)
+    return {"us_per_step": round(plain, 3),
+            "us_per_step_cuda_graph": None if graph_us is None else round(graph_us, 3),
+            "bytes_per_step": nbytes,
+            "achieved_gbs_graph": None if graph_us is None else round(nbytes / graph_us / 1e3, 1)}
+
+
+def oracle_tokens_per_s(w, x_cpu, budget_s):
+    """fp64 oracle (one core) on the first tokens of every head; returns (tok/s, sample)."""
+    from oracle import gdn_recurrent
+    H = w.Hv
+    # calibrate: a few tokens of every head
+    probe = 16
+    t = time.perf_counter()
+    sl = {k_: v_[:, :probe] for k_, v_ in x_cpu.items() if k_ in ("q", "k", "v", "g", "beta")}
+    gdn_recurrent(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, x_cpu["h0"][:1] if x_cpu["h0"] is not None else None)
+    per_tok = (time.perf_counter() - t) / probe
+    n_tok = int(max(probe, min(w.seqlens[0], budget_s / per_tok)))
+    sl = {k_: v_[:, :n_tok] for k_, v_ in x_cpu.items() if k_ in ("q", "k", "v", "g", "beta")}
+    h0 = x_cpu["h0"][:1] if x_cpu["h0"] is not None else None
+    t = time.perf_counter()
+    gdn_recurrent(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, h0)
+    dt = time.perf_counter() - t
+    return n_tok / dt, f"first {n_tok} tokens of sequence 0, all {H} v heads, fp64 numpy, 1 thread", dt
+
+
+def cpu_inputs(w, x):
+    """The same tensors on the host (first sequence row only) for the oracle legs."""
+    out = {}
+    for k_ in ("q", "k", "v", "g", "beta"):
+        out[k_] = x[k_][:1].detach().cpu()
+    out["h0"] = None if x["h0"] is None else x["h0"][:1].detach().cpu()
+    return out
+
+
+def bench_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    x = make_inputs(w, device="cpu")
+    xc = cpu_inputs(w, x)
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, xc, 0.05)
+    times, rates = [], []
+    sample = ""
+    for _ in range(args.steps):
+        r, sample, dt = oracle_tokens_per_s(w, xc, args.ref_step_s)
+        rates.append(r)
+        times.append(dt)
+    value = len(rates) / sum(1.0 / r for r in rates)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, 1), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_cuda(args, w, rank, world, local_rank):
+    import linear_attention_prefill_gb300 as lap
+    lap.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    x = make_inputs(w, device=dev, seed=rank_seed(w.seed, rank))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    o = torch.empty_like(x["v"])
+    hT = torch.empty((w.n_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
+
+    def step():
+        lap.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT,
+                          chunk=w.chunk, cu_seqlens=x["cu_seqlens"], stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.25)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    clk = clocks.stop()
+    local_ms = sum(ms)
+    job_ms, job_tokens = reduce_timing(local_ms, float(w.T_total * args.steps))
+    value = job_tokens / (job_ms / 1e3)
+    launches = args.steps  # one gdn_fwd kernel per step
+
+    # end to end through the public API from pinned host memory
+    host = {k_: (None if x[k_] is None else x[k_].detach().cpu().pin_memory())
+            for k_ in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")}
+    out = {}
+    for _ in range(max(1, args.warmup)):
+        lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 50))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    bi = bo = 0
+    for _ in range(e2e_steps):
+        o_h, hT_h, bi, bo = lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_ms, e2e_tok = reduce_timing(e2e_s * 1e3, float(w.T_total * e2e_steps))
+    e2e_value = e2e_tok / (e2e_ms / 1e3)
+
+    decode = run_decode(lap, w, dev) if args.decode else None
+
+    if rank != 0:
+        return
+    peaks, src = roofline.load_peaks()
+    model = roofline.workload_model(w, peaks)
+    avg_s = statistics.mean(ms) / 1e3
+    achieved = model["bytes"] / avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, world),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": measured_traffic(w.name), "peak_source": src,
+                     "kernel": KERNEL_NAME, "algorithmic_bytes": model["bytes"],
+                     "algorithmic_flops": model["flops"],
+                     "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),
+                     "t_roof_us": round(model["t_roof"] * 1e6, 2),
+                     "roofline_frac": round(model["t_roof"] / avg_s, 4)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernel_ms": {"median": statistics.median(ms), "min": min(ms), "max": max(ms)},
+    }
+    if decode is not None:
+        line["decode"] = decode
+    if world == 1 and args.cpu_baseline:
+        xc = cpu_inputs(w, x)
+        rate, sample, _ = oracle_tokens_per_s(w, xc, args.cpu_baseline_s)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    ap.add_argument("--ref-step-s", type=float, default=0.5)
+    ap.add_argument("--no-decode", dest="decode", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        bench_reference(args, w, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        bench_cuda(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,126 @@
+/*
+ * gdn.h - C ABI of libgdn.so: Gated DeltaNet chunked-prefill forward and the
+ * one-token decode step on an sm_103a GPU.
+ *
+ * The operation (per sequence n and value head hv, tokens t in order):
+ *
+ *     S_t = exp(g_t) * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t (scale * q_t)
+ *
+ * the gated delta rule of Gated DeltaNet, which "Empowering Hybrid Attention
+ * Models on NPUs" (§2.1, "Architecture of Linear-Attention Hybrids") describes
+ * as a fixed-size per-head state updated from K_t and V_t, then read with Q_t.
+ * The forward computes it chunkwise as that page's Map-Reduce-Map operators
+ * #1 Gate, #2 KKT, #3 Solve, #4 W/U, #5 H, #6 O (§2.1, Figure 1(b)), reading
+ * the state before updating it in place (§5, chunk-first order, Figure 10(b)).
+ * The state is stored transposed: h = S^T, [dk][dv] row-major.
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor pointer is DEVICE memory of the current device, dense
+ *    row-major in the stated shape, 16-byte aligned.  The caller owns every
+ *    buffer; the library allocates nothing and keeps no pointer after return.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  GDN_OK means the launch was enqueued.  Kernel faults
+ *    show up on the stream like any CUDA error.
+ *  - GQA: value head hv reads query/key head hv / (Hv / Hqk) ("grouped").
+ *  - q and k are expected L2-normalised per head vector, beta in (0, 1) and
+ *    g <= 0 (a log-decay); these are not checked.
+ *  - Errors: a non-OK status means nothing was launched (except GDN_ERR_CUDA,
+ *    which reports a failed launch).  gdn_last_error() gives a one-line
+ *    description, per calling thread.  Nothing prints, aborts or throws.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdn_stream_t; /* ABI-identical to cudaStream_t */
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer, Hv % Hqk != 0 */
+  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: dk, dv not in {64, 128}; chunk not in {64, 128} */
+  GDN_ERR_CUDA = 3,        /* a CUDA call failed (launch error, no device) */
+  GDN_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see gdn_device_status) */
+} gdn_status;
+
+/*
+ * gdn_chunk_fwd - chunked-prefill forward, bf16 q/k/v/o, fp32 gates and state.
+ *
+ *   q, k   [B, T, Hqk, dk] bf16       (with cu_seqlens: [1, T, Hqk, dk])
+ *   v      [B, T, Hv, dv]  bf16
+ *   g      [B, T, Hv] fp32  log-decay per token and value head
+ *   beta   [B, T, Hv] fp32
+ *   h0     [N, Hv, dk, dv] fp32 initial state, or NULL for zeros
+ *   o      [B, T, Hv, dv]  bf16 output (written; fp32 accumulation, rounded
+ *          to nearest even once)
+ *   hT     [N, Hv, dk, dv] fp32 final state, or NULL to skip; may equal h0
+ *          (each state tile is read before it is overwritten)
+ *   B      number of sequences N.  Without cu_seqlens the batch is B rows of
+ *          T tokens; with cu_seqlens it is one packed row of T tokens.
+ *   T      tokens per row (packed total with cu_seqlens); T = 0 is a no-op
+ *          that copies h0 (or zeros) to hT
+ *   chunk  chunk length C of the chunkwise form, 64 or 128; chunks restart at
+ *          every sequence start, the last one may be partial
+ *   scale  multiplies q (o_t = S_t (scale q_t)), usually dk^-0.5
+ *   cu_seqlens  NULL, or DEVICE int32 [B + 1]: 0 = cu[0] <= cu[1] <= ... <=
+ *          cu[B] = T (not checked on the host; empty sequences allowed)
+ *
+ * Supported: dk, dv in {64, 128}; Hv a multiple of Hqk.
+ */
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream);
+
+/* gdn_chunk_fwd_f32 - as gdn_chunk_fwd with fp32 q, k, v and o (fp32 throughout). */
+gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
+                             const float* beta, const float* h0, float* o, float* hT, int B,
+                             int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                             const int32_t* cu_seqlens, gdn_stream_t stream);
+
+/*
+ * gdn_recurrent_step - one decode token per sequence, continuing from a state
+ * (the rule above applied once; the decode path of "Empowering Hybrid
+ * Attention Models on NPUs", §7.3, and the per-token recurrence of "Exp
+ * 2026-07-13 — Linear-Attention Scans on the NPU", §4).
+ *
+ *   q, k  [N, Hqk, dk] bf16;  v [N, Hv, dv] bf16;  g, beta [N, Hv] fp32
+ *   h     [N, Hv, dk, dv] fp32, read and overwritten in place
+ *   o     [N, Hv, dv] bf16 output
+ */
+gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream);
+
+/* gdn_recurrent_step_f32 - as gdn_recurrent_step with fp32 q, k, v and o. */
+gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v,
+                                  const float* g, const float* beta, float* h, float* o, int N,
+                                  int Hqk, int Hv, int dk, int dv, float scale,
+                                  gdn_stream_t stream);
+
+/*
+ * gdn_device_status - waits for `stream`, then reads and clears the device
+ * error word that bounded device-side waits set when they give up.  Returns
+ * GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the stream itself failed.
+ */
+gdn_status gdn_device_status(gdn_stream_t stream);
+
+/* Static description of a status code. */
+const char* gdn_status_string(gdn_status s);
+
+/* Description of the last non-OK status returned to this thread ("" if none). */
+const char* gdn_last_error(void);
+
+/* ABI version of this header: 1. */
+int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

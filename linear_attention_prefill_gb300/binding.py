@@ -1,0 +1,217 @@
+"""Python binding of libgdn.so: argument marshalling only.
+
+The functions carry the C ABI's names.  They take torch tensors (device memory
+and streams are torch's), check dtypes, devices, shapes and contiguity, pass
+raw pointers and sizes to the library and turn a non-OK status into an
+exception.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback of any kind: without libgdn.so every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(5)
+
+# name -> (restype, argtypes) of every symbol include/gdn.h declares
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_FWD_ARGS = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]
+_STEP_ARGS = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]
+SIGNATURES = {
+    "gdn_chunk_fwd": (_I, _FWD_ARGS),
+    "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
+    "gdn_recurrent_step": (_I, _STEP_ARGS),
+    "gdn_recurrent_step_f32": (_I, _STEP_ARGS),
+    "gdn_device_status": (_I, [_P]),
+    "gdn_status_string": (ctypes.c_char_p, [_I]),
+    "gdn_last_error": (ctypes.c_char_p, []),
+    "gdn_abi_version": (_I, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{status_string(status)}: {detail}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgdn.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libgdn.so not found at {path}: build it first "
+                    "(python -m linear_attention_prefill_gb300._build)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().gdn_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, load_library().gdn_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t, name, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
+                  scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
+                  stream=None):
+    """Chunked-prefill forward; returns (o, hT).
+
+    q, k [B, T, Hqk, dk]; v [B, T, Hv, dv] (bf16 or fp32, all the same);
+    g, beta [B, T, Hv] fp32; h0 [N, Hv, dk, dv] fp32 or None.  With
+    cu_seqlens (int32 [N+1] on the device) the batch is one packed row, B = 1.
+    o and hT may be passed preallocated; hT may be h0 (in place).
+    """
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_chunk_fwd runs on a CUDA device")
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("q, k, v must be bf16 or fp32")
+    B, T, Hqk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    _need(q, "q", dt, dev)
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev, (B, T, Hv, dv))
+    _need(g, "g", torch.float32, dev, (B, T, Hv))
+    _need(beta, "beta", torch.float32, dev, (B, T, Hv))
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if B != 1:
+            raise ValueError("with cu_seqlens the batch must be one packed row (B == 1)")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev, (N, Hv, dk, dv))
+    if o is None:
+        o = torch.empty((B, T, Hv, dv), dtype=dt, device=dev)
+    _need(o, "o", dt, dev, (B, T, Hv, dv))
+    if hT is None and output_final_state:
+        hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
+    if hT is not None:
+        _need(hT, "hT", torch.float32, dev, (N, Hv, dk, dv))
+    if scale is None:
+        scale = dk ** -0.5
+    fn = lib.gdn_chunk_fwd if dt == torch.bfloat16 else lib.gdn_chunk_fwd_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
+              N, T, Hqk, Hv, dk, dv, chunk, float(scale), _ptr(cu_seqlens),
+              _stream_handle(stream, dev)))
+    return o, hT
+
+
+def gdn_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = None,
+                       stream=None):
+    """One decode token; updates h in place and returns o.
+
+    q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv] fp32; h [N, Hv, dk, dv] fp32.
+    """
+    lib = load_library()
+    dev = q.device
+    dt = q.dtype
+    N, Hqk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    _need(q, "q", dt, dev)
+    _need(k, "k", dt, dev, q.shape)
+    _need(v, "v", dt, dev, (N, Hv, dv))
+    _need(g, "g", torch.float32, dev, (N, Hv))
+    _need(beta, "beta", torch.float32, dev, (N, Hv))
+    _need(h, "h", torch.float32, dev, (N, Hv, dk, dv))
+    if o is None:
+        o = torch.empty((N, Hv, dv), dtype=dt, device=dev)
+    _need(o, "o", dt, dev, (N, Hv, dv))
+    if scale is None:
+        scale = dk ** -0.5
+    fn = lib.gdn_recurrent_step if dt == torch.bfloat16 else lib.gdn_recurrent_step_f32
+    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h), _ptr(o), N, Hqk, Hv,
+              dk, dv, float(scale), _stream_handle(stream, dev)))
+    return o
+
+
+def gdn_device_status(stream=None):
+    """Raise GdnError if a bounded device-side wait gave up since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load_library().gdn_device_status(_stream_handle(stream, dev)))
+
+
+def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None):
+    """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out.
+
+    ``inputs`` holds pinned CPU tensors q, k, v, g, beta and optionally h0 and
+    cu_seqlens.  ``out`` may hold preallocated pinned (o, hT) host tensors and
+    device buffers to reuse.  Returns (o_host, hT_host, bytes_in, bytes_out).
+    """
+    dev = torch.device(device)
+    bufs = out.setdefault("dev", {}) if out is not None else {}
+    d = {}
+    nbytes_in = 0
+    for name in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"):
+        t = inputs.get(name)
+        if t is None:
+            d[name] = None
+            continue
+        buf = bufs.get(name)
+        if buf is None or buf.shape != t.shape or buf.dtype != t.dtype:
+            buf = bufs[name] = torch.empty(t.shape, dtype=t.dtype, device=dev)
+        buf.copy_(t, non_blocking=True)
+        d[name] = buf
+        nbytes_in += t.numel() * t.element_size()
+    o_dev, hT_dev = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                                  bufs.get("o"), bufs.get("hT"), chunk=chunk,
+                                  cu_seqlens=d["cu_seqlens"], stream=stream)
+    bufs["o"], bufs["hT"] = o_dev, hT_dev
+    if out is not None and "o_host" in out:
+        o_h, hT_h = out["o_host"], out["hT_host"]
+    else:
+        o_h = torch.empty(o_dev.shape, dtype=o_dev.dtype, pin_memory=True)
+        hT_h = torch.empty(hT_dev.shape, dtype=hT_dev.dtype, pin_memory=True)
+        if out is not None:
+            out["o_host"], out["hT_host"] = o_h, hT_h
+    o_h.copy_(o_dev, non_blocking=True)
+    hT_h.copy_(hT_dev, non_blocking=True)
+    nbytes_out = o_h.numel() * o_h.element_size() + hT_h.numel() * hT_h.element_size()
+    return o_h, hT_h, nbytes_in, nbytes_out

@@ -1,0 +1,202 @@
+// gdn_abi.cu - the extern "C" boundary of libgdn.so (declared in include/gdn.h).
+//
+// Validates arguments, maps them onto launch parameters and enqueues the kernels
+// on the caller's stream.  It owns no tensors and allocates nothing.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+__device__ unsigned g_device_error = 0u;
+
+cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
+  unsigned zero = 0u;
+  cudaError_t err = cudaMemcpyFromSymbolAsync(out, g_device_error, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  if (err == cudaSuccess && *out != 0u)
+    err = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(unsigned), 0,
+                                  cudaMemcpyHostToDevice, stream);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+  return err;
+}
+
+}  // namespace gdn
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Shared validation of the forward; fills FwdParams.  elem = bytes of q/k/v/o.
+gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                     int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                     const int32_t* cu_seqlens, int elem, gdn::FwdParams* p) {
+  if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d and T=%d must be >= 0", B, T);
+  if (Hqk <= 0 || Hv <= 0) return fail(GDN_ERR_INVALID_ARG, "Hqk=%d, Hv=%d must be > 0", Hqk, Hv);
+  if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv=%d is not a multiple of Hqk=%d", Hv, Hqk);
+  if (!head_dim_ok(dk) || !head_dim_ok(dv))
+    return fail(GDN_ERR_UNSUPPORTED, "dk=%d, dv=%d: supported head dims are 64 and 128", dk, dv);
+  if (chunk != 64) return fail(GDN_ERR_UNSUPPORTED, "chunk=%d: supported chunk is 64", chunk);
+  if (!(scale == scale)) return fail(GDN_ERR_INVALID_ARG, "scale is NaN");
+  if (cu_seqlens && B < 1) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B >= 1 sequences");
+  const long long rows = cu_seqlens ? 1 : (long long)B;
+  const long long tokens = rows * (long long)T;
+  // every element index must fit comfortably in 63 bits and the grid in 2^31
+  if (tokens > (1ll << 40) || (long long)B * Hv * 2 > 0x7fffffffll)
+    return fail(GDN_ERR_INVALID_ARG, "problem too large: B=%d T=%d Hv=%d", B, T, Hv);
+  if (tokens > 0) {
+    if (!q || !k || !v || !g || !beta || !o)
+      return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta and o must be non-NULL when T > 0");
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(GDN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (!aligned(g, 4) || !aligned(beta, 4))
+    return fail(GDN_ERR_INVALID_ARG, "g and beta must be 4-byte aligned");
+  if (!aligned(h0, 16) || !aligned(hT, 16) || !aligned(cu_seqlens, 4))
+    return fail(GDN_ERR_INVALID_ARG, "h0 and hT must be 16-byte aligned, cu_seqlens 4-byte");
+  (void)elem;
+  p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->h0 = h0; p->o = o; p->hT = hT;
+  p->cu_seqlens = cu_seqlens;
+  p->N = B; p->T = T; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->chunk = chunk;
+  p->scale = scale;
+  return GDN_OK;
+}
+
+// T == 0 without cu_seqlens: no tokens, the final state is the initial one.
+gdn_status empty_forward(const gdn::FwdParams& p, cudaStream_t stream) {
+  if (!p.hT || p.N == 0) return GDN_OK;
+  const size_t bytes = (size_t)p.N * p.Hv * p.dk * p.dv * sizeof(float);
+  cudaError_t e = p.h0 ? (p.h0 == p.hT ? cudaSuccess
+                                       : cudaMemcpyAsync(p.hT, p.h0, bytes,
+                                                         cudaMemcpyDeviceToDevice, stream))
+                       : cudaMemsetAsync(p.hT, 0, bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copying h0 to hT");
+  return GDN_OK;
+}
+
+gdn_status check_step(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float* h, void* o, int N, int Hqk, int Hv, int dk,
+                      int dv, float scale, gdn::StepParams* p) {
+  if (N < 0) return fail(GDN_ERR_INVALID_ARG, "N=%d must be >= 0", N);
+  if (Hqk <= 0 || Hv <= 0) return fail(GDN_ERR_INVALID_ARG, "Hqk=%d, Hv=%d must be > 0", Hqk, Hv);
+  if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv=%d is not a multiple of Hqk=%d", Hv, Hqk);
+  if (!head_dim_ok(dk) || !head_dim_ok(dv))
+    return fail(GDN_ERR_UNSUPPORTED, "dk=%d, dv=%d: supported head dims are 64 and 128", dk, dv);
+  if (!(scale == scale)) return fail(GDN_ERR_INVALID_ARG, "scale is NaN");
+  if ((long long)N * Hv * 4 > 0x7fffffffll) return fail(GDN_ERR_INVALID_ARG, "N=%d too large", N);
+  if (N > 0 && (!q || !k || !v || !g || !beta || !h || !o))
+    return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta, h and o must be non-NULL");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(h, 16) || !aligned(g, 4) || !aligned(beta, 4))
+    return fail(GDN_ERR_INVALID_ARG, "misaligned pointer (16 bytes for tensors, 4 for g, beta)");
+  p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->h = h; p->o = o;
+  p->N = N; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->scale = scale;
+  return GDN_OK;
+}
+
+template <typename Launch>
+gdn_status run_fwd(const gdn::FwdParams& p, cudaStream_t stream, Launch launch) {
+  if (p.N == 0) return GDN_OK;
+  if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
+  cudaError_t e = launch(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd(p, reinterpret_cast<cudaStream_t>(stream), gdn::launch_fwd_bf16);
+}
+
+gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
+                             const float* beta, const float* h0, float* o, float* hT, int B,
+                             int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                             const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 4, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd(p, reinterpret_cast<cudaStream_t>(stream), gdn::launch_fwd_f32);
+}
+
+gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  if (N == 0) return GDN_OK;
+  cudaError_t e = gdn::launch_step_bf16(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
+}
+
+gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v,
+                                  const float* g, const float* beta, float* h, float* o, int N,
+                                  int Hqk, int Hv, int dk, int dv, float scale,
+                                  gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  if (N == 0) return GDN_OK;
+  cudaError_t e = gdn::launch_step_f32(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
+}
+
+gdn_status gdn_device_status(gdn_stream_t stream) {
+  unsigned word = 0u;
+  cudaError_t e = gdn::read_and_clear_device_error(&word, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word == gdn::kErrWaitTimeout)
+    return fail(GDN_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (word != 0u) return fail(GDN_ERR_TIMEOUT, "device error word 0x%x", word);
+  return GDN_OK;
+}
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+const char* gdn_last_error(void) { return t_last_error; }
+
+int gdn_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+// gdn_common.cuh - device helpers shared by the GDN kernels (sm_103a).
+//
+// Warp-level bf16 tensor-core fragments (mma.sync m16n8k16), ldmatrix loads,
+// cp.async staging, and the blocked unit-lower-triangular inverse used by the
+// #3 Solve operator of the chunkwise form ("Empowering Hybrid Attention Models
+// on NPUs", §2.1, Figure 1(b); the UT transform (I + A)^-1 of "Exp 2026-07-13
+// — Linear-Attention Scans on the NPU", §1).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Device error word: bounded waits record why they gave up (read by gdn_device_status).
+enum : unsigned { kErrNone = 0u, kErrWaitTimeout = 1u };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- cp.async (16-byte, zero-fill when src_bytes == 0) ----------------------
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, bool valid) {
+  const uint32_t d = smem_u32(smem_dst);
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gmem_src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src, bool valid) {
+  const uint32_t d = smem_u32(smem_dst);
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(gmem_src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---- ldmatrix ---------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                        const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                          const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+
+// D = A * B + D, bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment (16x16) of a row-major [m][k] bf16 tile at (m0, k0); ld in elements.
+__device__ __forceinline__ void load_a(uint32_t (&a)[4], const __nv_bfloat16* base, int ld,
+                                       int m0, int k0, int lane) {
+  const __nv_bfloat16* p = base + (m0 + (lane & 15)) * ld + k0 + ((lane >> 4) << 3);
+  ldsm_x4(a[0], a[1], a[2], a[3], p);
+}
+// A fragment (16x16) when the tile is stored transposed, as [k][m] (m contiguous).
+__device__ __forceinline__ void load_a_trans(uint32_t (&a)[4], const __nv_bfloat16* base, int ld,
+                                             int m0, int k0, int lane) {
+  // Stored as [k][m]; lane groups 0-7, 8-15, 16-23, 24-31 address the four 8x8
+  // matrices a0 (m 0-7, k 0-7), a1 (m 8-15, k 0-7), a2 (m 0-7, k 8-15),
+  // a3 (m 8-15, k 8-15); each row address is one k row of 8 m values.
+  const int g = lane >> 3;
+  const int kr = k0 + (lane & 7) + ((g >> 1) << 3);
+  const int mc = m0 + ((g & 1) << 3);
+  ldsm_x4_t(a[0], a[1], a[2], a[3], base + kr * ld + mc);
+}
+// Two B fragments (k16 x n8 each, n tiles n0 and n0+8) of a tile stored as [n][k]
+// (k contiguous): b[0],b[1] for n0; b[2],b[3] for n0+8.
+__device__ __forceinline__ void load_b_nk(uint32_t (&b)[4], const __nv_bfloat16* base, int ld,
+                                          int n0, int k0, int lane) {
+  const int g = lane >> 3;
+  const int nr = n0 + (lane & 7) + ((g >> 1) << 3);
+  const int kc = k0 + ((g & 1) << 3);
+  ldsm_x4(b[0], b[1], b[2], b[3], base + nr * ld + kc);
+}
+// Two B fragments of a tile stored as [k][n] (n contiguous).
+__device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __nv_bfloat16* base, int ld,
+                                          int n0, int k0, int lane) {
+  const int g = lane >> 3;
+  const int kr = k0 + (lane & 7) + ((g & 1) << 3);
+  const int nc = n0 + ((g >> 1) << 3);
+  ldsm_x4_t(b[0], b[1], b[2], b[3], base + kr * ld + nc);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---- blocked unit-lower-triangular inverse, 64 x 64, fp32 ------------------
+// T = (I + A)^-1 for strictly lower-triangular A (only its strictly lower part is
+// read).  Diagonal 16x16 blocks are inverted by forward substitution (one warp
+// per block, one lane per column); the off-diagonal blocks follow block row by
+// block row from T_IJ = -T_II * sum_{J<=M<I} A_IM T_MJ.  Called by all
+// NTHREADS threads of the block; X is 3*256 floats of scratch shared memory.
+template <int NTHREADS>
+__device__ __forceinline__ void solve_unit_lower_64(const float* A, int lda, float* T, int ldt,
+                                                    float* X) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  static_assert(NTHREADS >= 256, "solve needs 8 warps");
+  // zero the strictly upper blocks, set the diagonal blocks
+  if (warp < 4 && lane < 16) {
+    const int b = warp, l = lane;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s = (i == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) s -= A[(16 * b + i) * lda + 16 * b + m] * x[m];
+      x[i] = s;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) T[(16 * b + i) * ldt + 16 * b + l] = x[i];
+  } else if (warp >= 4) {
+    // upper blocks are zero
+    for (int e = tid - 128; e < 64 * 64; e += NTHREADS - 128) {
+      const int r = e >> 6, c = e & 63;
+      if ((c >> 4) > (r >> 4)) T[r * ldt + c] = 0.f;
+    }
+  }
+  __syncthreads();
+  for (int I = 1; I < 4; ++I) {
+    // X_J = sum_{M=J}^{I-1} A_IM T_MJ for J < I  (I blocks of 16x16)
+    for (int e = tid; e < I * 256; e += NTHREADS) {
+      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      float s = 0.f;
+      for (int M = J; M < I; ++M) {
+        const float* arow = A + (16 * I + r) * lda + 16 * M;
+        const float* tcol = T + (16 * M) * ldt + 16 * J + c;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s += arow[m] * tcol[m * ldt];
+      }
+      X[e] = s;
+    }
+    __syncthreads();
+    for (int e = tid; e < I * 256; e += NTHREADS) {
+      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      const float* trow = T + (16 * I + r) * ldt + 16 * I;
+      const float* xc = X + J * 256 + c;
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) s += (m <= r ? trow[m] : 0.f) * xc[m * 16];
+      T[(16 * I + r) * ldt + 16 * J + c] = -s;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace gdn

@@ -1,0 +1,102 @@
+// gdn_step.cu - one decode token: the gated delta rule applied once per
+// (sequence, v head), continuing from the state the prefill left behind
+// ("Empowering Hybrid Attention Models on NPUs", §7.3: decoding runs the
+// token-by-token recurrence; "Exp 2026-07-13 — Linear-Attention Scans on the
+// NPU", §4: the per-token recurrence needs no (I + A)^-1).
+//
+// Per token, with h = S^T of shape [dk, dv]:
+//   h <- exp(g) h;  u = beta (v - h^T k);  h <- h + k u^T;  o = h^T (scale q)
+// The state is read once and written once, so the step is bound by HBM
+// bandwidth: each CTA streams a [dk, 32] column tile of h with 128-byte
+// coalesced rows, keeps it in registers between the two column reductions.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kCols = 32;    // dv columns per CTA (one per lane)
+constexpr int kWarps = 4;    // warps split the dk rows
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <typename TIn, int DK>
+__global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams p) {
+  __shared__ float sk[DK], sq[DK];
+  __shared__ float red1[kWarps][kCols], red2[kWarps][kCols];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntile = p.dv / kCols;
+  const int tile = blockIdx.x % ntile;
+  const int hv = (blockIdx.x / ntile) % p.Hv;
+  const int n = blockIdx.x / (ntile * p.Hv);
+  const int hq = hv / (p.Hv / p.Hqk);
+  const TIn* q = static_cast<const TIn*>(p.q) + ((long long)n * p.Hqk + hq) * DK;
+  const TIn* k = static_cast<const TIn*>(p.k) + ((long long)n * p.Hqk + hq) * DK;
+  for (int i = tid; i < DK; i += kWarps * 32) {
+    sk[i] = to_f(k[i]);
+    sq[i] = to_f(q[i]) * p.scale;
+  }
+  const long long nh = (long long)n * p.Hv + hv;
+  const float alpha = expf(p.g[nh]);
+  const float b = p.beta[nh];
+  const int col = tile * kCols + lane;
+  const float vcol = to_f(static_cast<const TIn*>(p.v)[nh * p.dv + col]);
+  __syncthreads();
+
+  constexpr int R = DK / kWarps;  // rows per thread
+  float* h = p.h + nh * DK * p.dv + col;
+  float hr[R];
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int r = warp + kWarps * i;
+    hr[i] = alpha * h[(long long)r * p.dv];
+    part += hr[i] * sk[r];
+  }
+  red1[warp][lane] = part;
+  __syncthreads();
+  float kh = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) kh += red1[w][lane];
+  const float u = b * (vcol - kh);
+  part = 0.f;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int r = warp + kWarps * i;
+    hr[i] += sk[r] * u;
+    h[(long long)r * p.dv] = hr[i];
+    part += hr[i] * sq[r];
+  }
+  red2[warp][lane] = part;
+  __syncthreads();
+  if (warp == 0) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) o += red2[w][lane];
+    store(static_cast<TIn*>(p.o) + nh * p.dv + col, o);
+  }
+}
+
+template <typename TIn>
+cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
+  const long long grid = (long long)p.N * p.Hv * (p.dv / kCols);
+  if (p.dk == 128)
+    gdn_step_kernel<TIn, 128><<<(unsigned)grid, kWarps * 32, 0, stream>>>(p);
+  else
+    gdn_step_kernel<TIn, 64><<<(unsigned)grid, kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream) {
+  return launch_t<__nv_bfloat16>(p, stream);
+}
+cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream) {
+  return launch_t<float>(p, stream);
+}
+
+}  // namespace gdn

@@ -1,0 +1,87 @@
+"""Shared helpers for the GPU parity tests: run the oracle on chosen chains of the
+very tensors handed to the kernel, and the error measure of the tolerance."""
+import numpy as np
+import torch
+
+from oracle import gdn_recurrent, qk_head
+
+# max |x - x_ref| / RMS(x_ref): bf16 inputs with fp32 accumulation, and the fp32 path
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+
+
+def rel_err(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = np.sqrt(np.mean(ref ** 2))
+    if rms == 0.0:
+        return float(np.abs(x - ref).max())
+    return float(np.abs(x - ref).max() / rms)
+
+
+def to_np(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.numpy().astype(np.float64)
+
+
+def oracle_heads(x, heads, seqs=None):
+    """fp64 oracle for v heads ``heads`` (and sequences ``seqs``) of inputs ``x``.
+
+    Slices each chain's own q/k head (grouped GQA map) and v head so the oracle
+    touches only what it checks.  Returns {(n, hv): (o [L, dv], hT [dk, dv])}.
+    """
+    q, k, v, g, beta, h0, cu = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                                x["cu_seqlens"])
+    B, T, Hqk, _ = q.shape
+    Hv = v.shape[2]
+    if cu is None:
+        spans = [(b, b, 0, T) for b in range(B)]
+    else:
+        c = cu.cpu().numpy()
+        spans = [(n, 0, int(c[n]), int(c[n + 1])) for n in range(len(c) - 1)]
+    if seqs is not None:
+        spans = [spans[i] for i in seqs]
+    out = {}
+    for n, b, t0, t1 in spans:
+        for hv in heads:
+            hq = qk_head(hv, Hqk, Hv)
+            sl = slice(t0, t1)
+            h0n = None if h0 is None else to_np(h0[n:n + 1, hv:hv + 1])
+            o, hT = gdn_recurrent(to_np(q[b:b + 1, sl, hq:hq + 1]), to_np(k[b:b + 1, sl, hq:hq + 1]),
+                                  to_np(v[b:b + 1, sl, hv:hv + 1]), to_np(g[b:b + 1, sl, hv:hv + 1]),
+                                  to_np(beta[b:b + 1, sl, hv:hv + 1]), x["scale"], h0n)
+            out[(n, hv)] = (o[0, :, 0], hT[0, 0])
+    return out
+
+
+def check_heads(x, o, hT, heads, dtype, seqs=None, tol=None):
+    """Compare the kernel's o / hT with the oracle on the chosen chains; returns worst errors."""
+    tol = TOL[dtype] if tol is None else tol
+    ref = oracle_heads(x, heads, seqs)
+    cu = x["cu_seqlens"]
+    B, T = x["q"].shape[:2]
+    if cu is not None:
+        cu = cu.cpu().numpy()
+    spans = ([(b, b, 0, T) for b in range(B)] if cu is None else
+             [(n, 0, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)])
+    worst_o = worst_h = 0.0
+    o_parts, or_parts, h_parts, hr_parts = [], [], [], []
+    for (n, hv), (o_ref, h_ref) in ref.items():
+        _, b, t0, t1 = spans[n]
+        o_parts.append(to_np(o[b, t0:t1, hv]))
+        or_parts.append(o_ref)
+        if hT is not None:
+            h_parts.append(to_np(hT[n, hv]))
+            hr_parts.append(h_ref)
+    if o_parts:
+        worst_o = rel_err(np.concatenate([p.ravel() for p in o_parts]),
+                          np.concatenate([p.ravel() for p in or_parts]))
+    if h_parts:
+        worst_h = rel_err(np.concatenate([p.ravel() for p in h_parts]),
+                          np.concatenate([p.ravel() for p in hr_parts]))
+    assert worst_o <= tol, f"o error {worst_o:.3e} > {tol}"
+    assert worst_h <= tol, f"hT error {worst_h:.3e} > {tol}"
+    return worst_o, worst_h

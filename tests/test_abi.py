@@ -1,0 +1,122 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+rejects bad arguments before touching CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_prefill_gb300 import _build, binding
+    _build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_recurrent_step",
+                 "gdn_recurrent_step_f32", "gdn_status_string", "gdn_last_error",
+                 "gdn_device_status", "gdn_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from linear_attention_prefill_gb300.binding import SIGNATURES
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.gdn_abi_version() == 1
+    assert lib.gdn_status_string(0) == b"GDN_OK"
+    assert lib.gdn_status_string(1) == b"GDN_ERR_INVALID_ARG"
+    assert lib.gdn_status_string(2) == b"GDN_ERR_UNSUPPORTED"
+    assert lib.gdn_status_string(3) == b"GDN_ERR_CUDA"
+    assert lib.gdn_status_string(4) == b"GDN_ERR_TIMEOUT"
+
+
+A = 0x10000  # an aligned fake address: never dereferenced, validation fails first
+
+
+def fwd(lib, q=A, k=A, v=A, g=A, beta=A, h0=None, o=A, hT=None, B=1, T=128, Hqk=1, Hv=2,
+        dk=128, dv=128, chunk=64, scale=0.088, cu=None, f32=False):
+    fn = lib.gdn_chunk_fwd_f32 if f32 else lib.gdn_chunk_fwd
+    return fn(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale, cu, None)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+@pytest.mark.parametrize("case,status", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(g=None), 1),
+    (dict(beta=None), 1), (dict(o=None), 1),
+    (dict(B=-1), 1), (dict(T=-5), 1), (dict(Hqk=0), 1), (dict(Hv=0), 1),
+    (dict(Hqk=3, Hv=4), 1),
+    (dict(dk=96), 2), (dict(dv=32), 2), (dict(dk=256), 2), (dict(chunk=32), 2),
+    (dict(chunk=100), 2),
+    (dict(q=A + 8), 1), (dict(o=A + 2), 1), (dict(g=A + 2), 1), (dict(h0=A + 4), 1),
+    (dict(hT=A + 8), 1), (dict(cu=A + 2), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(T=1 << 30, B=4096), 1),
+    (dict(cu=A, B=0), 1),
+])
+def test_forward_rejects_bad_arguments(lib, case, status, f32):
+    assert fwd(lib, f32=f32, **case) == status
+    assert lib.gdn_last_error() != b""
+
+
+def step(lib, q=A, k=A, v=A, g=A, beta=A, h=A, o=A, N=2, Hqk=1, Hv=2, dk=128, dv=128,
+         scale=0.088, f32=False):
+    fn = lib.gdn_recurrent_step_f32 if f32 else lib.gdn_recurrent_step
+    return fn(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, None)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+@pytest.mark.parametrize("case,status", [
+    (dict(q=None), 1), (dict(h=None), 1), (dict(o=None), 1), (dict(N=-1), 1),
+    (dict(Hqk=2, Hv=3), 1), (dict(dk=80), 2), (dict(dv=256), 2), (dict(h=A + 4), 1),
+    (dict(scale=float("nan")), 1),
+])
+def test_step_rejects_bad_arguments(lib, case, status, f32):
+    assert step(lib, f32=f32, **case) == status
+
+
+def test_no_op_calls_return_ok_without_a_device(lib):
+    # B = 0 sequences and N = 0 decode rows enqueue nothing
+    assert fwd(lib, B=0, T=0, q=None, k=None, v=None, g=None, beta=None, o=None) == 0
+    assert step(lib, N=0, q=None, k=None, v=None, g=None, beta=None, h=None, o=None) == 0
+
+
+def test_binding_raises_without_the_library(tmp_path):
+    from linear_attention_prefill_gb300 import binding
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="libgdn.so not found"):
+            binding.load_library(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved
+
+
+def test_binding_signatures_cover_the_header():
+    from linear_attention_prefill_gb300.binding import SIGNATURES
+    assert sorted(SIGNATURES) == declared_functions()
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "linear_attention_prefill_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
