@@ -1,6 +1,6 @@
 // gdn_common.cuh - device helpers shared by the GDN kernels (sm_103a).
 //
-// Warp-level bf16 tensor-core fragments (mma.sync m16n8k16), ldmatrix loads,
+// Warp-level fp16 tensor-core fragments (mma.sync m16n8k16), ldmatrix loads,
 // cp.async staging, and the blocked unit-lower-triangular inverse used by the
 // #3 Solve operator of the chunkwise form ("Empowering Hybrid Attention Models
 // on NPUs", §2.1, Figure 1(b); the UT transform (I + A)^-1 of "Exp 2026-07-13
@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,24 +54,24 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& 
                : "r"(smem_u32(p)));
 }
 
-// D = A * B + D, bf16 inputs, fp32 accumulation.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
+// D = A * B + D, fp16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // A fragment (16x16) of a row-major [m][k] bf16 tile at (m0, k0); ld in elements.
-__device__ __forceinline__ void load_a(uint32_t (&a)[4], const __nv_bfloat16* base, int ld,
+__device__ __forceinline__ void load_a(uint32_t (&a)[4], const __half* base, int ld,
                                        int m0, int k0, int lane) {
-  const __nv_bfloat16* p = base + (m0 + (lane & 15)) * ld + k0 + ((lane >> 4) << 3);
+  const __half* p = base + (m0 + (lane & 15)) * ld + k0 + ((lane >> 4) << 3);
   ldsm_x4(a[0], a[1], a[2], a[3], p);
 }
 // A fragment (16x16) when the tile is stored transposed, as [k][m] (m contiguous).
-__device__ __forceinline__ void load_a_trans(uint32_t (&a)[4], const __nv_bfloat16* base, int ld,
+__device__ __forceinline__ void load_a_trans(uint32_t (&a)[4], const __half* base, int ld,
                                              int m0, int k0, int lane) {
   // Stored as [k][m]; lane groups 0-7, 8-15, 16-23, 24-31 address the four 8x8
   // matrices a0 (m 0-7, k 0-7), a1 (m 8-15, k 0-7), a2 (m 0-7, k 8-15),
@@ -82,7 +83,7 @@ __device__ __forceinline__ void load_a_trans(uint32_t (&a)[4], const __nv_bfloat
 }
 // Two B fragments (k16 x n8 each, n tiles n0 and n0+8) of a tile stored as [n][k]
 // (k contiguous): b[0],b[1] for n0; b[2],b[3] for n0+8.
-__device__ __forceinline__ void load_b_nk(uint32_t (&b)[4], const __nv_bfloat16* base, int ld,
+__device__ __forceinline__ void load_b_nk(uint32_t (&b)[4], const __half* base, int ld,
                                           int n0, int k0, int lane) {
   const int g = lane >> 3;
   const int nr = n0 + (lane & 7) + ((g >> 1) << 3);
@@ -90,7 +91,7 @@ __device__ __forceinline__ void load_b_nk(uint32_t (&b)[4], const __nv_bfloat16*
   ldsm_x4(b[0], b[1], b[2], b[3], base + nr * ld + kc);
 }
 // Two B fragments of a tile stored as [k][n] (n contiguous).
-__device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __nv_bfloat16* base, int ld,
+__device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __half* base, int ld,
                                           int n0, int k0, int lane) {
   const int g = lane >> 3;
   const int kr = k0 + (lane & 7) + ((g & 1) << 3);
@@ -101,6 +102,26 @@ __device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __nv_bfloat16*
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Eight bf16 values at p (16-byte aligned, shared memory) rewritten in place as
+// fp16.  Exact for |x| in [2^-14, 65504]; smaller magnitudes keep an absolute
+// error below 2^-25.
+__device__ __forceinline__ void bf16x8_to_f16x8(void* p) {
+  uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  uint4 out;
+  __half2* h = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(b[i]);
+    h[i] = __floats2half2_rn(f.x, f.y);
+  }
+  *reinterpret_cast<uint4*>(p) = out;
 }
 
 // ---- blocked unit-lower-triangular inverse, 64 x 64, fp32 ------------------

@@ -18,10 +18,13 @@
 // column split of the state for parallelism without a reduction (§4,
 // Figure 8(b)) decide the grid: one CTA per (sequence, v head, dv tile).
 //
-// Contractions run on bf16 tensor cores (mma.sync m16n8k16, fp32 accumulate);
-// the bf16 operands are q, k, v as given, Tm scaled by beta (gamma), W, V_new,
-// e*V_new and a bf16 copy of the fp32 state.  Chunk tiles are staged into
-// padded shared memory with cp.async, double-buffered one chunk ahead.
+// Contractions run on fp16 tensor cores (mma.sync m16n8k16, fp32 accumulate).
+// The bf16 q/k/v tiles are rewritten as fp16 once staged (exact in fp16's
+// normal range), and every on-chip operand (Tm scaled by beta (gamma), W,
+// V_new, e*V_new, the state copy, P) is fp16: its 11-bit significand keeps the
+// operand rounding 8x below bf16's at the same tensor-core rate.  The fp32
+// state itself never leaves the registers until the end.  Chunk tiles are staged
+// into padded shared memory with cp.async, double-buffered one chunk ahead.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -33,26 +36,26 @@ constexpr int kThreads = 256;   // 8 warps
 
 template <int DK, int DVT>
 struct SmemBf16 {
-  static constexpr int LDK = DK + 8;   // bf16 row stride of K, Q, -W (272 B for DK=128)
-  static constexpr int LDV = DVT + 8;  // bf16 row stride of V, V_new, e*V_new, h
-  static constexpr int LDC = kC + 8;   // bf16 row stride of the 64x64 Tw, Tu, P
+  static constexpr int LDK = DK + 8;   // 16-bit row stride of K, Q, -W (272 B for DK=128)
+  static constexpr int LDV = DVT + 8;  // 16-bit row stride of V, V_new, e*V_new, h
+  static constexpr int LDC = kC + 8;   // 16-bit row stride of the 64x64 Tw, Tu, P
   static constexpr int LDA = kC + 4;   // fp32 row stride of A and Tm
-  __nv_bfloat16 K[2][kC * LDK];
-  __nv_bfloat16 Q[2][kC * LDK];
-  __nv_bfloat16 V[2][kC * LDV];
+  __half K[2][kC * LDK];   // staged as bf16, converted in place to fp16
+  __half Q[2][kC * LDK];
+  __half V[2][kC * LDV];
   float g[2][kC];
   float beta[2][kC];
   float G[kC], gam[kC], e[kC];
   float A[kC * LDA];
   float Tm[kC * LDA];
   float X[3 * 256];
-  __nv_bfloat16 Tw[kC * LDC];
-  __nv_bfloat16 Tu[kC * LDC];
-  __nv_bfloat16 P[kC * LDC];
-  __nv_bfloat16 Wn[kC * LDK];  // -W
-  __nv_bfloat16 H[DK * LDV];   // bf16 copy of the state tile
-  __nv_bfloat16 Vn[kC * LDV];  // V_new
-  __nv_bfloat16 Ve[kC * LDV];  // diag(e) V_new
+  __half Tw[kC * LDC];
+  __half Tu[kC * LDC];
+  __half P[kC * LDC];
+  __half Wn[kC * LDK];  // -W
+  __half H[DK * LDV];   // fp16 copy of the state tile
+  __half Vn[kC * LDV];  // V_new
+  __half Ve[kC * LDV];  // diag(e) V_new
 };
 
 template <int DK, int DVT>
@@ -137,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
         b = *reinterpret_cast<const float2*>(h0 + (long long)(r0 + 8) * p.dv + col);
       }
       hacc[j][0] = a.x; hacc[j][1] = a.y; hacc[j][2] = b.x; hacc[j][3] = b.y;
-      *reinterpret_cast<uint32_t*>(&s.H[r0 * LDV + col]) = pack_bf16(a.x, a.y);
-      *reinterpret_cast<uint32_t*>(&s.H[(r0 + 8) * LDV + col]) = pack_bf16(b.x, b.y);
+      *reinterpret_cast<uint32_t*>(&s.H[r0 * LDV + col]) = pack_f16(a.x, a.y);
+      *reinterpret_cast<uint32_t*>(&s.H[(r0 + 8) * LDV + col]) = pack_f16(b.x, b.y);
     }
   }
 
@@ -154,8 +157,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
       cp_async_wait<0>();
     }
     __syncthreads();
-    const __nv_bfloat16* Ks = s.K[buf];
-    const __nv_bfloat16* Qs = s.Q[buf];
+    // bf16 -> fp16 in place (16 bytes per thread per step), then every product is fp16
+    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
+      const int r = i / (DK / 8), sg = i % (DK / 8);
+      bf16x8_to_f16x8(&s.K[buf][r * LDK + sg * 8]);
+      bf16x8_to_f16x8(&s.Q[buf][r * LDK + sg * 8]);
+    }
+    for (int i = tid; i < kC * (DVT / 8); i += kThreads) {
+      const int r = i / (DVT / 8), sg = i % (DVT / 8);
+      bf16x8_to_f16x8(&s.V[buf][r * LDV + sg * 8]);
+    }
+    __syncthreads();
+    const __half* Ks = s.K[buf];
+    const __half* Qs = s.Q[buf];
 
     // ---- #1 Gate (padded rows carry g = 0, so G[kC-1] = G[L-1]) ----------
     if (warp == 0) {
@@ -193,16 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
           load_a(ak, Ks, LDK, 16 * rb, kk, lane);
           load_a(aq, Qs, LDK, 16 * rb, kk, lane);
           load_b_nk(b, Ks, LDK, 32 * ch, kk, lane);
-          mma_bf16(aK[0], ak, b[0], b[1]);
-          mma_bf16(aK[1], ak, b[2], b[3]);
-          mma_bf16(aQ[0], aq, b[0], b[1]);
-          mma_bf16(aQ[1], aq, b[2], b[3]);
+          mma_f16(aK[0], ak, b[0], b[1]);
+          mma_f16(aK[1], ak, b[2], b[3]);
+          mma_f16(aQ[0], aq, b[0], b[1]);
+          mma_f16(aQ[1], aq, b[2], b[3]);
           if (need1) {
             load_b_nk(b, Ks, LDK, 32 * ch + 16, kk, lane);
-            mma_bf16(aK[2], ak, b[0], b[1]);
-            mma_bf16(aK[3], ak, b[2], b[3]);
-            mma_bf16(aQ[2], aq, b[0], b[1]);
-            mma_bf16(aQ[3], aq, b[2], b[3]);
+            mma_f16(aK[2], ak, b[0], b[1]);
+            mma_f16(aK[3], ak, b[2], b[3]);
+            mma_f16(aQ[2], aq, b[0], b[1]);
+            mma_f16(aQ[3], aq, b[2], b[3]);
           }
         }
       }
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
           const bool low = r >= cc && r < L;
           const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
           s.A[r * LDA + cc] = (low && r > cc) ? s.beta[buf][r] * m * aK[j][x] : 0.f;
-          s.P[r * LDC + cc] = __float2bfloat16_rn(low ? p.scale * m * aQ[j][x] : 0.f);
+          s.P[r * LDC + cc] = __float2half_rn(low ? p.scale * m * aQ[j][x] : 0.f);
         }
       }
     }
@@ -227,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
       const int r = e >> 6, cc = e & 63;
       const float tv = s.Tm[r * LDA + cc];
       const float b = s.beta[buf][cc];
-      s.Tw[r * LDC + cc] = __float2bfloat16_rn(tv * b * s.gam[cc]);
-      s.Tu[r * LDC + cc] = __float2bfloat16_rn(tv * b);
+      s.Tw[r * LDC + cc] = __float2half_rn(tv * b * s.gam[cc]);
+      s.Tu[r * LDC + cc] = __float2half_rn(tv * b);
     }
     __syncthreads();
 
@@ -253,23 +267,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
         for (int j = 0; j < WNT; j += 2) {
           load_b_kn(b, Ks, LDK, nq * (DK / 2) + 8 * j, kk, lane);
-          mma_bf16(aW[j], a, b[0], b[1]);
-          mma_bf16(aW[j + 1], a, b[2], b[3]);
+          mma_f16(aW[j], a, b[0], b[1]);
+          mma_f16(aW[j + 1], a, b[2], b[3]);
         }
         load_a(a, s.Tu, LDC, 16 * rb, kk, lane);
 #pragma unroll
         for (int j = 0; j < UNT; j += 2) {
           load_b_kn(b, s.V[buf], LDV, nq * (DVT / 2) + 8 * j, kk, lane);
-          mma_bf16(acc[j], a, b[0], b[1]);
-          mma_bf16(acc[j + 1], a, b[2], b[3]);
+          mma_f16(acc[j], a, b[0], b[1]);
+          mma_f16(acc[j + 1], a, b[2], b[3]);
         }
       }
 #pragma unroll
       for (int j = 0; j < WNT; ++j) {
         const int r0 = 16 * rb + gq, col = nq * (DK / 2) + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&s.Wn[r0 * LDK + col]) = pack_bf16(-aW[j][0], -aW[j][1]);
+        *reinterpret_cast<uint32_t*>(&s.Wn[r0 * LDK + col]) = pack_f16(-aW[j][0], -aW[j][1]);
         *reinterpret_cast<uint32_t*>(&s.Wn[(r0 + 8) * LDK + col]) =
-            pack_bf16(-aW[j][2], -aW[j][3]);
+            pack_f16(-aW[j][2], -aW[j][3]);
       }
     }
     __syncthreads();
@@ -282,8 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
       for (int j = 0; j < UNT; j += 2) {
         load_b_kn(b, s.H, LDV, nq * (DVT / 2) + 8 * j, kk, lane);
-        mma_bf16(acc[j], a, b[0], b[1]);
-        mma_bf16(acc[j + 1], a, b[2], b[3]);
+        mma_f16(acc[j], a, b[0], b[1]);
+        mma_f16(acc[j + 1], a, b[2], b[3]);
       }
     }
     {
@@ -292,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
       for (int j = 0; j < UNT; ++j) {
         const int col = nq * (DVT / 2) + 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&s.Vn[r0 * LDV + col]) = pack_bf16(acc[j][0], acc[j][1]);
+        *reinterpret_cast<uint32_t*>(&s.Vn[r0 * LDV + col]) = pack_f16(acc[j][0], acc[j][1]);
         *reinterpret_cast<uint32_t*>(&s.Vn[(r0 + 8) * LDV + col]) =
-            pack_bf16(acc[j][2], acc[j][3]);
+            pack_f16(acc[j][2], acc[j][3]);
         *reinterpret_cast<uint32_t*>(&s.Ve[r0 * LDV + col]) =
-            pack_bf16(e0 * acc[j][0], e0 * acc[j][1]);
+            pack_f16(e0 * acc[j][0], e0 * acc[j][1]);
         *reinterpret_cast<uint32_t*>(&s.Ve[(r0 + 8) * LDV + col]) =
-            pack_bf16(e1 * acc[j][2], e1 * acc[j][3]);
+            pack_f16(e1 * acc[j][2], e1 * acc[j][3]);
       }
     }
     __syncthreads();
@@ -316,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
         for (int j = 0; j < UNT; j += 2) {
           load_b_kn(b, s.H, LDV, nq * (DVT / 2) + 8 * j, kk, lane);
-          mma_bf16(acc[j], a, b[0], b[1]);
-          mma_bf16(acc[j + 1], a, b[2], b[3]);
+          mma_f16(acc[j], a, b[0], b[1]);
+          mma_f16(acc[j + 1], a, b[2], b[3]);
         }
       }
       const int r0 = 16 * rb + gq;
@@ -332,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
         for (int j = 0; j < UNT; j += 2) {
           load_b_kn(b, s.Vn, LDV, nq * (DVT / 2) + 8 * j, kk, lane);
-          mma_bf16(acc[j], a, b[0], b[1]);
-          mma_bf16(acc[j + 1], a, b[2], b[3]);
+          mma_f16(acc[j], a, b[0], b[1]);
+          mma_f16(acc[j + 1], a, b[2], b[3]);
         }
       }
 #pragma unroll
@@ -362,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
         for (int j = 0; j < HNT; j += 2) {
           load_b_kn(b, s.Ve, LDV, hcol0 + 8 * j, kk, lane);
-          mma_bf16(hacc[j], a, b[0], b[1]);
-          mma_bf16(hacc[j + 1], a, b[2], b[3]);
+          mma_f16(hacc[j], a, b[0], b[1]);
+          mma_f16(hacc[j + 1], a, b[2], b[3]);
         }
       }
     }
@@ -371,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_bf16_kernel(const FwdPara
 #pragma unroll
     for (int j = 0; j < HNT; ++j) {
       const int r0 = 16 * hmt + gq, col = hcol0 + 8 * j + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&s.H[r0 * LDV + col]) = pack_bf16(hacc[j][0], hacc[j][1]);
-      *reinterpret_cast<uint32_t*>(&s.H[(r0 + 8) * LDV + col]) = pack_bf16(hacc[j][2], hacc[j][3]);
+      *reinterpret_cast<uint32_t*>(&s.H[r0 * LDV + col]) = pack_f16(hacc[j][0], hacc[j][1]);
+      *reinterpret_cast<uint32_t*>(&s.H[(r0 + 8) * LDV + col]) = pack_f16(hacc[j][2], hacc[j][3]);
     }
     __syncthreads();  // buffers of this chunk are free, s.H holds the new state
   }

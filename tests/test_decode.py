@@ -22,7 +22,7 @@ def test_single_step(cuda_lib, dtype, dk, dv):
     o = cuda_lib.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], h)
     torch.cuda.synchronize()
     o_ref, h_ref = gdn_step(x["q"], x["k"], x["v"], x["g"], x["beta"], h_before, x["scale"])
-    assert rel_err(to_np(o), o_ref) < TOL[dtype]
+    assert rel_err(to_np(o), o_ref, out_dtype=dtype) < TOL[dtype]
     assert rel_err(to_np(h), h_ref) < TOL[dtype]
 
 
@@ -43,7 +43,7 @@ def test_prefill_then_decode(cuda_lib, dtype):
     o_ref, h_ref = gdn_recurrent(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"], x["scale"],
                                  x["h0"])
     o_dec = torch.stack(outs, dim=1)
-    assert rel_err(to_np(o_dec), o_ref[:, 200:]) < TOL[dtype]
+    assert rel_err(to_np(o_dec), o_ref[:, 200:], out_dtype=dtype) < TOL[dtype]
     assert rel_err(to_np(h), h_ref) < TOL[dtype]
 
 
@@ -75,4 +75,4 @@ def test_long_context_then_1000_steps(cuda_lib):
     b = np.array([float(s_["beta"]) for s_ in steps])
     o_ref = recurrent_chain(q, k, v, g, b, chain, w.scale)
     assert rel_err(to_np(h[0, hv]), chain) < TOL["bf16"]
-    assert rel_err(to_np(o_last[0, hv]), o_ref[-1]) < TOL["bf16"]
+    assert rel_err(to_np(o_last[0, hv]), o_ref[-1], out_dtype="bf16") < TOL["bf16"]

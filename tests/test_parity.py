@@ -4,7 +4,8 @@ Small cases compare every element; the full-size workloads (launched exactly as
 bench.py launches them) compare every token of sampled (sequence, v head)
 chains, which the oracle computes one by one.  Tolerance: max |x - ref| /
 RMS(ref) <= 2e-2 for bf16 inputs with fp32 accumulation, 1e-4 for the fp32
-path, on o and on the final state.
+path, on o and on the final state.  A bf16 o is first allowed the half-ulp
+rounding of its own store (helpers.rel_err); the fp32 state gets no allowance.
 """
 import numpy as np
 import pytest
@@ -130,7 +131,7 @@ def test_pure_decay_when_beta_is_zero(cuda_lib, dtype):
     h0 = x["h0"][0].double()                                          # [Hv, dk, dv]
     q = x["q"][0].double()                                            # [T, Hqk, dk]
     want = torch.einsum("thd,hdv->thv", q[:, [0, 0]] * x["scale"], h0) * torch.exp(G)[..., None]
-    assert rel_err(to_np(o[0]), want.cpu().numpy()) < TOL[dtype]
+    assert rel_err(to_np(o[0]), want.cpu().numpy(), out_dtype=dtype) < TOL[dtype]
     assert rel_err(to_np(hT[0]), (torch.exp(G[-1])[:, None, None] * h0).cpu().numpy()) < TOL[dtype]
 
 
