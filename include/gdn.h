@@ -18,7 +18,8 @@
  * Conventions shared by every entry point
  *  - Every tensor pointer is DEVICE memory of the current device, dense
  *    row-major in the stated shape, 16-byte aligned.  The caller owns every
- *    buffer; the library allocates nothing and keeps no pointer after return.
+ *    buffer; the library keeps no pointer and no allocation after a call
+ *    (only gdn_chunk_fwd takes a temporary workspace, see gdn_chunk_fwd_ex).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  GDN_OK means the launch was enqueued.  Kernel faults
  *    show up on the stream like any CUDA error.
@@ -32,6 +33,7 @@
 #ifndef GDN_H_
 #define GDN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -43,7 +45,7 @@ typedef struct CUstream_st* gdn_stream_t; /* ABI-identical to cudaStream_t */
 typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer, Hv % Hqk != 0 */
-  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: dk, dv not in {64, 128}; chunk not in {64, 128} */
+  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: dk, dv not in {64, 128}; chunk != 64 */
   GDN_ERR_CUDA = 3,        /* a CUDA call failed (launch error, no device) */
   GDN_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see gdn_device_status) */
 } gdn_status;
@@ -64,7 +66,7 @@ typedef enum {
  *          T tokens; with cu_seqlens it is one packed row of T tokens.
  *   T      tokens per row (packed total with cu_seqlens); T = 0 is a no-op
  *          that copies h0 (or zeros) to hT
- *   chunk  chunk length C of the chunkwise form, 64 or 128; chunks restart at
+ *   chunk  chunk length C of the chunkwise form (64); chunks restart at
  *          every sequence start, the last one may be partial
  *   scale  multiplies q (o_t = S_t (scale q_t)), usually dk^-0.5
  *   cu_seqlens  NULL, or DEVICE int32 [B + 1]: 0 = cu[0] <= cu[1] <= ... <=
@@ -77,7 +79,35 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          int Hqk, int Hv, int dk, int dv, int chunk, float scale,
                          const int32_t* cu_seqlens, gdn_stream_t stream);
 
-/* gdn_chunk_fwd_f32 - as gdn_chunk_fwd with fp32 q, k, v and o (fp32 throughout). */
+/*
+ * gdn_chunk_fwd_workspace_size - bytes of device workspace gdn_chunk_fwd_ex
+ * needs for these sizes (has_cu_seqlens: 1 if cu_seqlens will be passed).
+ * The bf16 forward runs in three launches: the chunk-parallel operators #1-#4
+ * (Gate, KKT, Solve, W/U) write a per-(chunk, v head) record (W, diag(e) K,
+ * diag(scale gamma) Q, P, U: fp16), the chunk-serial #5 H launch adds the state
+ * entering each chunk and V_new, and the chunk-parallel #6 O launch reads them:
+ * 120 KB per chunk and v head at d = 128.  Returns 0 for sizes gdn_chunk_fwd
+ * would reject.
+ */
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
+                                    int has_cu_seqlens);
+
+/*
+ * gdn_chunk_fwd_ex - gdn_chunk_fwd with a caller-provided device workspace of
+ * at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte aligned.  The
+ * workspace is overwritten; calls sharing it must be ordered on one stream.
+ * Returns GDN_ERR_INVALID_ARG if it is NULL, misaligned or too small.
+ * (gdn_chunk_fwd itself takes the workspace from the device's stream-ordered
+ * memory pool with cudaMallocAsync/cudaFreeAsync on `stream`.)
+ */
+gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream);
+
+/* gdn_chunk_fwd_f32 - as gdn_chunk_fwd with fp32 q, k, v and o (fp32 throughout).
+ * One fused launch per call; no workspace. */
 gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
                              const float* beta, const float* h0, float* o, float* hT, int B,
                              int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,

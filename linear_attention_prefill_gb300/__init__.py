@@ -4,8 +4,9 @@ The compute lives in libgdn.so (``csrc/``, C ABI in ``include/gdn.h``); this
 package holds the Python binding with the ABI's names, the seeded synthetic
 workloads and the algorithmic byte/FLOP model.
 """
-from .binding import (GdnError, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_device_status,
-                      gdn_recurrent_step, load_library, status_string)
+from .binding import (GdnError, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_workspace_size,
+                      gdn_device_status, gdn_recurrent_step, load_library, status_string)
 
-__all__ = ["GdnError", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_device_status",
+__all__ = ["GdnError", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_workspace_size",
+           "gdn_device_status",
            "gdn_recurrent_step", "load_library", "status_string"]

@@ -24,8 +24,11 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT 
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _FWD_ARGS = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]
 _STEP_ARGS = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]
+_SZ = ctypes.c_size_t
 SIGNATURES = {
     "gdn_chunk_fwd": (_I, _FWD_ARGS),
+    "gdn_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "gdn_chunk_fwd_workspace_size": (_SZ, [_I] * 8),
     "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
     "gdn_recurrent_step": (_I, _STEP_ARGS),
     "gdn_recurrent_step_f32": (_I, _STEP_ARGS),
@@ -95,15 +98,24 @@ def _need(t, name, dtype, device, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+def gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) -> int:
+    """Bytes of workspace the bf16 forward needs (0 for rejected sizes)."""
+    return int(load_library().gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk,
+                                                           int(bool(varlen))))
+
+
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
-                  stream=None):
+                  stream=None, workspace=None):
     """Chunked-prefill forward; returns (o, hT).
 
     q, k [B, T, Hqk, dk]; v [B, T, Hv, dv] (bf16 or fp32, all the same);
     g, beta [B, T, Hv] fp32; h0 [N, Hv, dk, dv] fp32 or None.  With
     cu_seqlens (int32 [N+1] on the device) the batch is one packed row, B = 1.
-    o and hT may be passed preallocated; hT may be h0 (in place).
+    o and hT may be passed preallocated; hT may be h0 (in place).  The bf16
+    path runs gdn_chunk_fwd_ex with ``workspace`` (a uint8 device tensor of at
+    least gdn_chunk_fwd_workspace_size bytes) or a fresh one from torch's
+    caching allocator.
     """
     lib = load_library()
     dev = q.device
@@ -137,10 +149,17 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
         _need(hT, "hT", torch.float32, dev, (N, Hv, dk, dv))
     if scale is None:
         scale = dk ** -0.5
-    fn = lib.gdn_chunk_fwd if dt == torch.bfloat16 else lib.gdn_chunk_fwd_f32
-    _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
-              N, T, Hqk, Hv, dk, dv, chunk, float(scale), _ptr(cu_seqlens),
-              _stream_handle(stream, dev)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
+            N, T, Hqk, Hv, dk, dv, chunk, float(scale), _ptr(cu_seqlens))
+    if dt == torch.float32:
+        _check(lib.gdn_chunk_fwd_f32(*args, _stream_handle(stream, dev)))
+        return o, hT
+    need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk, cu_seqlens is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    _check(lib.gdn_chunk_fwd_ex(*args, _ptr(workspace), workspace.numel(),
+                                _stream_handle(stream, dev)))
     return o, hT
 
 
@@ -202,7 +221,8 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         nbytes_in += t.numel() * t.element_size()
     o_dev, hT_dev = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
                                   bufs.get("o"), bufs.get("hT"), chunk=chunk,
-                                  cu_seqlens=d["cu_seqlens"], stream=stream)
+                                  cu_seqlens=d["cu_seqlens"], stream=stream,
+                                  workspace=bufs.get("workspace"))
     bufs["o"], bufs["hT"] = o_dev, hT_dev
     if out is not None and "o_host" in out:
         o_h, hT_h = out["o_host"], out["hT_host"]

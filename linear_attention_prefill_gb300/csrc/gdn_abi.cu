@@ -116,18 +116,58 @@ gdn_status check_step(const void* q, const void* k, const void* v, const float* 
   return GDN_OK;
 }
 
-template <typename Launch>
-gdn_status run_fwd(const gdn::FwdParams& p, cudaStream_t stream, Launch launch) {
+gdn_status run_fwd_f32(const gdn::FwdParams& p, cudaStream_t stream) {
   if (p.N == 0) return GDN_OK;
   if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
-  cudaError_t e = launch(p, stream);
+  cudaError_t e = gdn::launch_fwd_f32(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");
+  return GDN_OK;
+}
+
+// bf16 forward: chunk-parallel prep launch, chunk-serial chain launch, chunk-parallel output launch.
+gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaStream_t stream) {
+  if (p.N == 0) return GDN_OK;
+  if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
+  const gdn::WsLayout w = gdn::ws_layout(p, ws);
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % 256) != 0 || ws_size < gdn::ws_bytes(w, p.Hv))
+    return fail(GDN_ERR_INVALID_ARG, "workspace %p of %zu bytes: need %zu bytes, 256-byte aligned",
+                ws, ws_size, gdn::ws_bytes(w, p.Hv));
+  cudaError_t e = gdn::launch_prep(p, w, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
+  e = gdn::launch_chain(p, w, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the chain kernel");
+  e = gdn::launch_out(p, w, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the output kernel");
   return GDN_OK;
 }
 
 }  // namespace
 
 extern "C" {
+
+gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
+                                    int has_cu_seqlens) {
+  gdn::FwdParams p;
+  static const int32_t fake_cu = 0;
+  const void* A = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (check_fwd(A, A, A, static_cast<const float*>(A), static_cast<const float*>(A), nullptr,
+                const_cast<void*>(A), nullptr, B, T, Hqk, Hv, dk, dv, chunk, 1.0f,
+                has_cu_seqlens ? &fake_cu : nullptr, 2, &p) != GDN_OK)
+    return 0;
+  return gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+}
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, const float* h0, void* o, float* hT, int B, int T,
@@ -137,7 +177,16 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
-  return run_fwd(p, reinterpret_cast<cudaStream_t>(stream), gdn::launch_fwd_bf16);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (p.N == 0 || (!cu_seqlens && T == 0)) return run_fwd_bf16(p, nullptr, 0, st);
+  const size_t bytes = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "allocating the workspace");
+  s = run_fwd_bf16(p, ws, bytes, st);
+  e = cudaFreeAsync(ws, st);
+  if (s == GDN_OK && e != cudaSuccess) return cuda_fail(e, "freeing the workspace");
+  return s;
 }
 
 gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
@@ -148,7 +197,7 @@ gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, con
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 4, &p);
   if (s != GDN_OK) return s;
-  return run_fwd(p, reinterpret_cast<cudaStream_t>(stream), gdn::launch_fwd_f32);
+  return run_fwd_f32(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_f32_kernel(const FwdParam
     __syncthreads();
 
     // #3 Solve
-    solve_unit_lower_64<kThreads>(s.A, LDA, s.Tm, LDA, s.X);
+    solve_unit_lower_64_f32<kThreads>(s.A, LDA, s.Tm, LDA, s.X);
 
     // #5 read (rewritten): R = diag(beta) V - diag(beta gamma) K h   -> s.A
     //   and the inter-chunk part of #6: O1 = diag(scale gamma) Q h     -> registers

@@ -1,6 +1,7 @@
 // gdn_internal.h - launch parameters shared by the C ABI layer and the kernels.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,8 +37,111 @@ struct StepParams {
   float scale;
 };
 
+// Workspace of the bf16 forward: one record per (chunk slot, v head), all fp16
+// row-major unless stated:
+//   W    [64][dk]         Tm diag(beta gamma) K                  (gdn_prep)
+//   Kt   [64][dk]         diag(e) K, e_j = exp(G_last - G_j)     (gdn_prep)
+//   Qt   [64][dk]         diag(scale gamma) Q                    (gdn_prep)
+//   P    [64][64]         tril(scale exp(G_i - G_j) q_i.k_j)     (gdn_prep)
+//   U    [dv/32][64][32]  Tm diag(beta) V, one block per 32-column dv tile (gdn_prep)
+//   gl   fp32 + pad       gamma_last = exp(G_last)               (gdn_prep)
+//   H    [dv/32][dk][32]  state entering the chunk, per dv tile  (gdn_chain)
+//   Vn   [dv/32][64][32]  V_new = U - W h, per dv tile           (gdn_chain)
+// gdn_out reads Qt, P, H and Vn.  Sequence n's chunk c lives in slot
+// first_slot(n) + c: n * ceil(T / 64) for fixed-length rows; floor(cu[n] / 64) +
+// n with cu_seqlens, which never overlaps because floor((a + L) / 64) -
+// floor(a / 64) + 1 >= ceil(L / 64), and ends below floor(T / 64) + N + 1.
+constexpr int kChunk = 64;
+constexpr int kDvTile = 32;  // dv columns per chain CTA
+
+struct WsLayout {
+  char* base;
+  long long n_slots;        // chunk slots per v head
+  long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
+  long long task_bytes, kt_off, qt_off, p_off, u_off, gl_off, h_off, vn_off;
+
+  __host__ __device__ char* rec(long long slot, int hv, int Hv) const {
+    return base + (slot * Hv + hv) * task_bytes;
+  }
+  __host__ __device__ __half* W(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv));
+  }
+  __host__ __device__ __half* Kt(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + kt_off);
+  }
+  __host__ __device__ __half* Qt(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + qt_off);
+  }
+  __host__ __device__ __half* P(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + p_off);
+  }
+  __host__ __device__ __half* U(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + u_off);
+  }
+  __host__ __device__ float* gl(long long s, int hv, int Hv) const {
+    return reinterpret_cast<float*>(rec(s, hv, Hv) + gl_off);
+  }
+  __host__ __device__ __half* H(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + h_off);
+  }
+  __host__ __device__ __half* Vn(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + vn_off);
+  }
+  __device__ long long first_slot(const FwdParams& p, int n) const {
+    if (p.cu_seqlens) return (long long)(p.cu_seqlens[n] / kChunk) + n;
+    return (long long)n * slots_per_seq;
+  }
+};
+
+// Layout for one call (sizes validated); base may be null when only sizing.
+inline WsLayout ws_layout(const FwdParams& p, void* base) {
+  WsLayout w;
+  w.base = static_cast<char*>(base);
+  if (p.cu_seqlens) {
+    w.slots_per_seq = 0;
+    w.n_slots = (long long)p.T / kChunk + p.N + 1;
+  } else {
+    w.slots_per_seq = ((long long)p.T + kChunk - 1) / kChunk;
+    w.n_slots = w.slots_per_seq * p.N;
+  }
+  const long long wk = (long long)kChunk * p.dk * 2, wv = (long long)kChunk * p.dv * 2;
+  w.kt_off = wk;
+  w.qt_off = 2 * wk;
+  w.p_off = 3 * wk;
+  w.u_off = w.p_off + (long long)kChunk * kChunk * 2;
+  w.gl_off = w.u_off + wv;
+  w.h_off = w.gl_off + 16;
+  w.vn_off = w.h_off + (long long)p.dk * p.dv * 2;
+  w.task_bytes = w.vn_off + wv;
+  return w;
+}
+inline size_t ws_bytes(const WsLayout& w, int Hv) { return (size_t)(w.n_slots * Hv * w.task_bytes); }
+
+// Slot -> (sequence, chunk of that sequence); false for a slot no chunk uses.
+__device__ inline bool locate_chunk(const FwdParams& p, const WsLayout& ws, long long slot, int* n,
+                                    int* c) {
+  if (!p.cu_seqlens) {
+    *n = (int)(slot / ws.slots_per_seq);
+    *c = (int)(slot % ws.slots_per_seq);
+    return *n < p.N;
+  }
+  int lo = 0, hi = p.N - 1;  // largest n with first_slot(n) <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)(p.cu_seqlens[mid] / kChunk) + mid <= slot) lo = mid; else hi = mid - 1;
+  }
+  const long long first = (long long)(p.cu_seqlens[lo] / kChunk) + lo;
+  const long long len = (long long)p.cu_seqlens[lo + 1] - p.cu_seqlens[lo];
+  if (slot < first || slot - first >= (len + kChunk - 1) / kChunk) return false;
+  *n = lo;
+  *c = (int)(slot - first);
+  return true;
+}
+
 // Launchers: return cudaSuccess or the launch error.  Each validates nothing.
-cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+cudaError_t launch_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream);
 cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream);

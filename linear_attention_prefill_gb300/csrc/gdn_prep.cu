@@ -1,0 +1,301 @@
+// gdn_prep.cu - the chunk-parallel Map phase of the chunkwise forward.
+//
+// "Empowering Hybrid Attention Models on NPUs", §2.1, Figure 1(b): operators
+// #1-#4 (Gate, KKT, Solve, W/U) depend only on one chunk's q, k, v, g, beta,
+// so every (chunk, v head) is an independent task here:
+//   #1 Gate   G = cumsum(g), gamma = exp(G), e_j = exp(G_last - G_j)
+//   #2 KKT    A = tril_strict(beta_i exp(G_i - G_j) k_i.k_j)
+//      QK^T   P = tril(scale exp(G_i - G_j) q_i.k_j)
+//   #3 Solve  Tm = (I + A)^-1   (diagonal blocks by substitution, merges on tensor cores)
+//   #4 W/U    W = Tm diag(beta gamma) K,  U = Tm diag(beta) V
+// plus the two scaled copies the later launches consume: Kt = diag(e) K (the
+// state update's left factor) and Qt = diag(scale gamma) Q (the output's
+// inter-chunk term).  The serial Reduce (#5) runs in gdn_chain.cu, the final
+// Map (#6) in gdn_out.cu; both read this kernel's workspace records.
+//
+// Tensor-core products use fp16 operands with fp32 accumulation (q, k, v are
+// staged as bf16 and rewritten in place as fp16, exact in fp16's normal range).
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kC = 64;
+constexpr int kThreads = 256;
+
+template <int DK, int DV>
+struct PrepSmem {
+  static constexpr int LDK = DK + 8;   // 16-bit row strides (conflict-free ldmatrix)
+  static constexpr int LDV = DV + 8;
+  static constexpr int LDC = kC + 8;
+  static constexpr int LDA = kC + 4;   // fp32 row stride of A and Tm
+  __half K[kC * LDK];
+  union {                              // Q until the grams are done, then A, then U staging
+    __half Q[kC * LDK];
+    float A[kC * LDA];
+    __half Ust[kC * LDV];
+  };
+  __half V[kC * LDV];
+  union {                              // Tm until Tw/Tu are built, then W staging
+    float Tm[kC * LDA];
+    __half Wst[kC * LDK];
+  };
+  __half Ah[kC * LDC];
+  __half Th[kC * LDC];
+  __half Tw[kC * LDC];
+  __half Tu[kC * LDC];
+  float g[kC], beta[kC], G[kC], gam[kC], e[kC];
+};
+
+// 8 fp16 values at p (16-byte aligned) times `scale`, rounded once.
+__device__ __forceinline__ uint4 scale_f16x8(const __half* p, float scale) {
+  uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __half2* h = reinterpret_cast<const __half2*>(&raw);
+  uint4 out;
+  __half2* o = reinterpret_cast<__half2*>(&out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    o[i] = __floats2half2_rn(f.x * scale, f.y * scale);
+  }
+  return out;
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p, WsLayout ws) {
+  using S = PrepSmem<DK, DV>;
+  constexpr int LDK = S::LDK, LDV = S::LDV, LDC = S::LDC, LDA = S::LDA;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  S& s = *reinterpret_cast<S*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+
+  // task -> (chunk slot, v head) -> (sequence, chunk within it)
+  const int hv = blockIdx.x % p.Hv;
+  const long long slot = blockIdx.x / p.Hv;
+  int n, c;
+  if (!locate_chunk(p, ws, slot, &n, &c)) return;
+  const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
+  const long long len =
+      p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
+  const long long t0 = t_seq + (long long)c * kC;
+  const int L = (int)min((long long)kC, len - (long long)c * kC);
+  const int hq = hv / (p.Hv / p.Hqk);
+
+  // ---- staging (cp.async, zero-filled past the sequence end) ---------------
+  {
+    const long long qk_tok = (long long)p.Hqk * DK, v_tok = (long long)p.Hv * DV;
+    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k) + (long long)hq * DK;
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + (long long)hq * DK;
+    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v) + (long long)hv * DV;
+    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
+      const int r = i / (DK / 8), sg = i % (DK / 8);
+      const bool ok = r < L;
+      const long long tok = t0 + (ok ? r : 0);
+      cp_async16(&s.K[r * LDK + sg * 8], kg + tok * qk_tok + sg * 8, ok);
+      cp_async16(&s.Q[r * LDK + sg * 8], qg + tok * qk_tok + sg * 8, ok);
+    }
+    for (int i = tid; i < kC * (DV / 8); i += kThreads) {
+      const int r = i / (DV / 8), sg = i % (DV / 8);
+      const bool ok = r < L;
+      const long long tok = t0 + (ok ? r : 0);
+      cp_async16(&s.V[r * LDV + sg * 8], vg + tok * v_tok + sg * 8, ok);
+    }
+    if (tid < kC) {
+      const bool ok = tid < L;
+      const long long tok = t0 + (ok ? tid : 0);
+      cp_async4(&s.g[tid], p.g + tok * p.Hv + hv, ok);
+      cp_async4(&s.beta[tid], p.beta + tok * p.Hv + hv, ok);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  for (int i = tid; i < kC * (DK / 8); i += kThreads) {
+    const int r = i / (DK / 8), sg = i % (DK / 8);
+    bf16x8_to_f16x8(&s.K[r * LDK + sg * 8]);
+    bf16x8_to_f16x8(&s.Q[r * LDK + sg * 8]);
+  }
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {
+    const int r = i / (DV / 8), sg = i % (DV / 8);
+    bf16x8_to_f16x8(&s.V[r * LDV + sg * 8]);
+  }
+  // ---- #1 Gate (padded rows carry g = 0, so G[63] = G_last) ------------------
+  if (warp == 0) {
+    const float g0 = s.g[2 * lane], g1 = s.g[2 * lane + 1];
+    float incl = g0 + g1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const float Glast = __shfl_sync(0xffffffffu, incl, 31);
+    s.G[2 * lane] = incl - g1;
+    s.G[2 * lane + 1] = incl;
+    s.gam[2 * lane] = expf(incl - g1);
+    s.gam[2 * lane + 1] = expf(incl);
+    s.e[2 * lane] = expf(Glast - (incl - g1));
+    s.e[2 * lane + 1] = expf(Glast - incl);
+    if (lane == 31) *ws.gl(slot, hv, p.Hv) = expf(Glast);
+  }
+  __syncthreads();
+
+  // ---- #2 KKT and QK^T grams (lower triangle) -------------------------------
+  __half* Pout = ws.P(slot, hv, p.Hv);
+  {
+    const int rb = warp >> 1, ch = warp & 1;
+    float aK[4][4], aQ[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) aK[j][x] = aQ[j][x] = 0.f;
+    const bool need0 = 2 * ch <= rb, need1 = 2 * ch + 1 <= rb;
+    if (need0) {
+#pragma unroll 2
+      for (int kk = 0; kk < DK; kk += 16) {
+        uint32_t ak[4], aq[4], b[4];
+        load_a(ak, s.K, LDK, 16 * rb, kk, lane);
+        load_a(aq, s.Q, LDK, 16 * rb, kk, lane);
+        load_b_nk(b, s.K, LDK, 32 * ch, kk, lane);
+        mma_f16(aK[0], ak, b[0], b[1]);
+        mma_f16(aK[1], ak, b[2], b[3]);
+        mma_f16(aQ[0], aq, b[0], b[1]);
+        mma_f16(aQ[1], aq, b[2], b[3]);
+        if (need1) {
+          load_b_nk(b, s.K, LDK, 32 * ch + 16, kk, lane);
+          mma_f16(aK[2], ak, b[0], b[1]);
+          mma_f16(aK[3], ak, b[2], b[3]);
+          mma_f16(aQ[2], aq, b[0], b[1]);
+          mma_f16(aQ[3], aq, b[2], b[3]);
+        }
+      }
+    }
+    // the scaled copies Qt = diag(scale gamma) Q and Kt = diag(e) K
+    __half* Qt = ws.Qt(slot, hv, p.Hv);
+    __half* Kt = ws.Kt(slot, hv, p.Hv);
+    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
+      const int r = i / (DK / 8), sg = i % (DK / 8);
+      *reinterpret_cast<uint4*>(Qt + r * DK + sg * 8) =
+          scale_f16x8(&s.Q[r * LDK + sg * 8], p.scale * s.gam[r]);
+      *reinterpret_cast<uint4*>(Kt + r * DK + sg * 8) = scale_f16x8(&s.K[r * LDK + sg * 8], s.e[r]);
+    }
+    __syncthreads();  // Q is dead: its storage becomes A
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int x = 0; x < 4; x += 2) {
+        const int r = 16 * rb + gq + ((x >> 1) << 3);
+        const int c0 = 32 * ch + 8 * j + 2 * tq;
+        float pv[2], av[2];
+#pragma unroll
+        for (int y = 0; y < 2; ++y) {
+          const int cc = c0 + y;
+          const bool low = r >= cc && r < L;
+          const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
+          av[y] = (low && r > cc) ? s.beta[r] * m * aK[j][x + y] : 0.f;
+          pv[y] = low ? p.scale * m * aQ[j][x + y] : 0.f;
+          s.A[r * LDA + cc] = av[y];
+        }
+        *reinterpret_cast<uint32_t*>(&s.Ah[r * LDC + c0]) = pack_f16(av[0], av[1]);
+        *reinterpret_cast<uint32_t*>(Pout + r * kC + c0) = pack_f16(pv[0], pv[1]);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- #3 Solve and the scaled fp16 operands --------------------------------
+  solve_unit_lower_64(s.A, LDA, s.Ah, s.Tm, LDA, s.Th, LDC);
+  for (int e = tid; e < kC * kC; e += kThreads) {
+    const int r = e >> 6, cc = e & 63;
+    const float tv = s.Tm[r * LDA + cc];
+    const float b = s.beta[cc];
+    s.Tw[r * LDC + cc] = __float2half_rn(tv * b * s.gam[cc]);
+    s.Tu[r * LDC + cc] = __float2half_rn(tv * b);
+  }
+  __syncthreads();
+
+  // ---- #4 W = Tw K, U = Tu V (lower-triangular Tw/Tu: k <= row block) -------
+  {
+    const int rb = warp & 3, nh = warp >> 2;
+    constexpr int WNT = DK / 16, UNT = DV / 16;  // n8 tiles per warp (half the columns)
+    float aW[WNT][4], aU[UNT][4];
+#pragma unroll
+    for (int j = 0; j < WNT; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) aW[j][x] = 0.f;
+#pragma unroll
+    for (int j = 0; j < UNT; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) aU[j][x] = 0.f;
+    for (int kk = 0; kk <= 16 * rb; kk += 16) {
+      uint32_t a[4], b[4];
+      load_a(a, s.Tw, LDC, 16 * rb, kk, lane);
+#pragma unroll
+      for (int j = 0; j < WNT; j += 2) {
+        load_b_kn(b, s.K, LDK, nh * (DK / 2) + 8 * j, kk, lane);
+        mma_f16(aW[j], a, b[0], b[1]);
+        mma_f16(aW[j + 1], a, b[2], b[3]);
+      }
+      load_a(a, s.Tu, LDC, 16 * rb, kk, lane);
+#pragma unroll
+      for (int j = 0; j < UNT; j += 2) {
+        load_b_kn(b, s.V, LDV, nh * (DV / 2) + 8 * j, kk, lane);
+        mma_f16(aU[j], a, b[0], b[1]);
+        mma_f16(aU[j + 1], a, b[2], b[3]);
+      }
+    }
+    __syncthreads();  // Tm and A/Q storage are dead: stage W and U there
+    const int r0 = 16 * rb + gq;
+#pragma unroll
+    for (int j = 0; j < WNT; ++j) {
+      const int col = nh * (DK / 2) + 8 * j + 2 * tq;
+      *reinterpret_cast<uint32_t*>(&s.Wst[r0 * LDK + col]) = pack_f16(aW[j][0], aW[j][1]);
+      *reinterpret_cast<uint32_t*>(&s.Wst[(r0 + 8) * LDK + col]) = pack_f16(aW[j][2], aW[j][3]);
+    }
+#pragma unroll
+    for (int j = 0; j < UNT; ++j) {
+      const int col = nh * (DV / 2) + 8 * j + 2 * tq;
+      *reinterpret_cast<uint32_t*>(&s.Ust[r0 * LDV + col]) = pack_f16(aU[j][0], aU[j][1]);
+      *reinterpret_cast<uint32_t*>(&s.Ust[(r0 + 8) * LDV + col]) = pack_f16(aU[j][2], aU[j][3]);
+    }
+  }
+  __syncthreads();
+  __half* Wout = ws.W(slot, hv, p.Hv);
+  __half* Uout = ws.U(slot, hv, p.Hv);
+  for (int i = tid; i < kC * (DK / 8); i += kThreads) {
+    const int r = i / (DK / 8), sg = i % (DK / 8);
+    *reinterpret_cast<uint4*>(Wout + r * DK + sg * 8) =
+        *reinterpret_cast<const uint4*>(&s.Wst[r * LDK + sg * 8]);
+  }
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // U tile-major: [dv/32][64][32]
+    const int r = i / (DV / 8), sg = i % (DV / 8);
+    const int col = sg * 8, t = col / kDvTile, w = col % kDvTile;
+    *reinterpret_cast<uint4*>(Uout + (t * kC + r) * kDvTile + w) =
+        *reinterpret_cast<const uint4*>(&s.Ust[r * LDV + col]);
+  }
+}
+
+template <int DK, int DV>
+cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  const size_t smem = sizeof(PrepSmem<DK, DV>);
+  cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK, DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long grid = ws.n_slots * p.Hv;
+  gdn_prep_kernel<DK, DV><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  if (p.dk == 128) {
+    if (p.dv == 128) return launch_t<128, 128>(p, ws, stream);
+    return launch_t<128, 64>(p, ws, stream);
+  }
+  if (p.dv == 128) return launch_t<64, 128>(p, ws, stream);
+  return launch_t<64, 64>(p, ws, stream);
+}
+
+}  // namespace gdn

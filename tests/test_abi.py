@@ -120,3 +120,26 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_workspace_size_formula(lib):
+    # record: W, Kt, Qt [64][dk], P [64][64], U [64][dv], 16 B, H [dk][dv], Vn [64][dv] (fp16)
+    def rec(dk, dv):
+        return 3 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 16 + dk * dv * 2 + 64 * dv * 2
+    # fixed-length rows: N * ceil(T/64) slots x Hv records
+    assert lib.gdn_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == 64 * 16 * rec(128, 128)
+    assert lib.gdn_chunk_fwd_workspace_size(2, 100, 1, 4, 128, 64, 64, 0) == 2 * 2 * 4 * rec(128, 64)
+    # packed rows: floor(T/64) + N + 1 slots
+    assert lib.gdn_chunk_fwd_workspace_size(8, 9849, 16, 32, 128, 128, 64, 1) == (9849 // 64 + 9) * 32 * rec(128, 128)
+    # rejected sizes give 0
+    assert lib.gdn_chunk_fwd_workspace_size(1, 64, 3, 4, 128, 128, 64, 0) == 0
+    assert lib.gdn_chunk_fwd_workspace_size(1, 64, 1, 1, 96, 128, 64, 0) == 0
+
+
+def test_ex_rejects_small_or_misaligned_workspace(lib):
+    need = lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
+    args = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
+    assert lib.gdn_chunk_fwd_ex(*args, None, need, None) == 1
+    assert lib.gdn_chunk_fwd_ex(*args, A, need - 1, None) == 1
+    assert lib.gdn_chunk_fwd_ex(*args, A + 16, need, None) == 1
+    assert b"workspace" in lib.gdn_last_error()

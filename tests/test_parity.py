@@ -175,3 +175,22 @@ def test_workload(cuda_lib, name):
     print(f"{name}: err_o={eo:.3e} err_h={eh:.3e}")
     # properties that hold at any size: finite everywhere
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+
+
+def test_allocating_entry_point_matches_workspace_entry_point(cuda_lib):
+    """gdn_chunk_fwd (stream-ordered workspace) == gdn_chunk_fwd_ex, bit for bit."""
+    import ctypes
+    lib = cuda_lib.load_library()
+    w = small(0, Hqk=2, Hv=4, seqlens=[70, 0, 130], seed=18)
+    x = make_inputs(w, device="cuda")
+    o_ref, h_ref = run(cuda_lib, x)
+    o = torch.empty_like(o_ref)
+    h = torch.empty_like(h_ref)
+    st = torch.cuda.current_stream().cuda_stream
+    rc = lib.gdn_chunk_fwd(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                           x["g"].data_ptr(), x["beta"].data_ptr(), x["h0"].data_ptr(),
+                           o.data_ptr(), h.data_ptr(), 3, x["q"].shape[1], 2, 4, 128, 128, 64,
+                           ctypes.c_float(x["scale"]), x["cu_seqlens"].data_ptr(), st)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert torch.equal(o, o_ref) and torch.equal(h, h_ref)
