@@ -10,6 +10,10 @@
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
+#ifdef GDN_PROFILE
+__device__ unsigned long long g_gdn_phase[64];
+#endif
+
 namespace gdn {
 
 __device__ unsigned g_device_error = 0u;
@@ -79,6 +83,7 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   (void)elem;
   p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->h0 = h0; p->o = o; p->hT = hT;
   p->cu_seqlens = cu_seqlens;
+  p->err = nullptr;
   p->N = B; p->T = T; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->chunk = chunk;
   p->scale = scale;
   return GDN_OK;
@@ -124,6 +129,8 @@ gdn_status run_fwd_f32(const gdn::FwdParams& p, cudaStream_t stream) {
   return GDN_OK;
 }
 
+gdn_status launch_three(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream);
+
 // bf16 forward: chunk-parallel prep launch, chunk-serial chain launch, chunk-parallel output launch.
 gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaStream_t stream) {
   if (p.N == 0) return GDN_OK;
@@ -132,6 +139,13 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % 256) != 0 || ws_size < gdn::ws_bytes(w, p.Hv))
     return fail(GDN_ERR_INVALID_ARG, "workspace %p of %zu bytes: need %zu bytes, 256-byte aligned",
                 ws, ws_size, gdn::ws_bytes(w, p.Hv));
+  gdn::FwdParams q = p;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&q.err), gdn::g_device_error);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the device error word");
+  return launch_three(q, w, stream);
+}
+
+gdn_status launch_three(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
   cudaError_t e = gdn::launch_prep(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
   e = gdn::launch_chain(p, w, stream);

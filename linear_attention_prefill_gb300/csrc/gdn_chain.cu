@@ -3,14 +3,18 @@
 // §5 (Figure 10(b)) into the state read and the in-place update:
 //   #5 read    V_new = U - W h
 //   #5 update  h = gamma_last h + Kt^T V_new        (Kt = diag(e) K)
-// One CTA per (sequence, v head, 32-column dv tile) walks the chunks of its
-// sequence in order with its fp32 state tile h[:, tile] in registers: the
-// column split of the state (§4, Figure 8(b)) gives parallelism without any
-// reduction.  Per chunk it reads only W, Kt and its U tile (36 KB at d = 128,
-// about what one SM can pull from L2 in a chain step) from gdn_prep's record,
-// and publishes the state entering the chunk (H) and V_new for gdn_out, which
-// forms the outputs chunk-parallel.  The chain's two products are warp-level
-// fp16 tensor-core MMAs (mma.sync; the state is their accumulator).
+// One CTA per (sequence, v head, dv tile) walks the chunks of its sequence in
+// order with its fp32 state tile h[:, tile] in registers: the column split of
+// the state (§4, Figure 8(b)) gives parallelism without any reduction.
+//
+// Warp roles.  Warps 0-3 run the chain: two warp-level fp16 tensor-core
+// products per chunk (mma.sync, the state as accumulator) and two CTA-local
+// barriers - nothing else sits on the serial path.  Warp 4 is the producer: it
+// stages W, Kt, the U tile and gamma_last of chunk c + 3 with bulk copies into a
+// 3-deep ring (36 KB per chunk at d = 128: one SM takes in about 64 bytes per
+// clock from L2, which bounds the step), and publishes the state entering each
+// chunk (H) and V_new with bulk stores for gdn_out.  The roles meet only at
+// mbarriers; every wait is bounded and an expired wait ends the CTA cleanly.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -18,36 +22,40 @@ namespace gdn {
 namespace {
 
 constexpr int kC = 64;
-constexpr int kThreads = 128;  // 4 warps
+constexpr int kComputeThreads = 128;  // warps 0-3
+constexpr int kThreads = 160;         // + producer warp
 constexpr int kStages = 3;
-constexpr int DVT = kDvTile;
 
-template <int DK>
+template <int DK, int DVT>
 struct ChainSmem {
-  static constexpr int LDK = DK + 8;
-  static constexpr int LDT = DVT + 8;
   struct Stage {
-    __half W[kC * LDK];
-    __half Kt[kC * LDK];
-    __half U[kC * LDT];
+    __half W[kC * DK];    // swz<DK>
+    __half Kt[kC * DK];   // swz<DK>
+    __half U[kC * DVT];   // plain
     float gl[4];
   };
   Stage st[kStages];
-  __half H[DK * LDT];     // fp16 copy of the state tile entering the chunk
-  __half Vn[kC * LDT];    // V_new
+  __half H[2][DK * DVT];   // swz<DVT>: state entering the chunk (double-buffered for the store)
+  __half Vn[2][kC * DVT];  // swz<DVT>
+  uint64_t full[kStages];  // producer -> chain: chunk staged (transaction bytes)
+  uint64_t empty[kStages]; // chain -> producer: stage consumed (4 warp arrivals)
+  uint64_t pub[2];         // chain -> producer: H[b], Vn[b] ready to store
+  uint64_t pubd[2];        // producer -> chain: H[b], Vn[b] read by the store
+  int abort;
 };
 
-template <int DK>
+template <int DK, int DVT>
 __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams p, WsLayout ws) {
-  using S = ChainSmem<DK>;
-  constexpr int LDK = S::LDK, LDT = S::LDT;
-  constexpr int NT = DVT / 8;          // n8 tiles over the dv tile (4)
+  using S = ChainSmem<DK, DVT>;
+  constexpr int NT = DVT / 8;          // n8 tiles over the dv tile
   constexpr int MTW = DK / 64;         // m16 tiles of the state per warp
+  constexpr unsigned kStageBytes = 2 * kC * DK * 2 + kC * DVT * 2 + 16;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
+  GDN_PHASE_INIT;
   const int n_dvt = p.dv / DVT;
   const int dvt = blockIdx.x % n_dvt;
   const int hv = (blockIdx.x / n_dvt) % p.Hv;
@@ -57,29 +65,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
   const int n_chunks = (int)((len + kC - 1) / kC);
   const long long slot0 = ws.first_slot(p, n);
 
-  auto issue = [&](int c) {
-    if (c < n_chunks) {
-      typename S::Stage& b = s.st[c % kStages];
-      const __half* Wg = ws.W(slot0 + c, hv, p.Hv);
-      const __half* Kg = ws.Kt(slot0 + c, hv, p.Hv);
-      const __half* Ug = ws.U(slot0 + c, hv, p.Hv) + dvt * kC * DVT;
-      for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-        const int r = i / (DK / 8), sg = i % (DK / 8);
-        cp_async16(&b.W[r * LDK + sg * 8], Wg + r * DK + sg * 8, true);
-        cp_async16(&b.Kt[r * LDK + sg * 8], Kg + r * DK + sg * 8, true);
-      }
-      for (int i = tid; i < kC * (DVT / 8); i += kThreads) {
-        const int r = i / (DVT / 8), sg = i % (DVT / 8);
-        cp_async16(&b.U[r * LDT + sg * 8], Ug + r * DVT + sg * 8, true);
-      }
-      if (tid == 0) cp_async4(&b.gl[0], ws.gl(slot0 + c, hv, p.Hv), true);
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 4);
     }
-    cp_async_commit();  // possibly empty: one group per chunk keeps the counting uniform
-  };
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.pub[i], 1);
+      mbar_init(&s.pubd[i], 1);
+    }
+    s.abort = 0;
+    mbar_fence_init();
+  }
 
-  // ---- initial state ---------------------------------------------------------
+  // ---- initial state (chain warps) --------------------------------------------
   float hacc[MTW][NT][4];
-  {
+  if (warp < 4) {
     const float* h0 =
         p.h0 ? p.h0 + ((long long)(n * p.Hv + hv) * DK) * p.dv + dvt * DVT : nullptr;
 #pragma unroll
@@ -93,28 +94,54 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
           b = *reinterpret_cast<const float2*>(h0 + (long long)(r0 + 8) * p.dv + col);
         }
         hacc[mt][j][0] = a.x; hacc[mt][j][1] = a.y; hacc[mt][j][2] = b.x; hacc[mt][j][3] = b.y;
-        *reinterpret_cast<uint32_t*>(&s.H[r0 * LDT + col]) = pack_f16(a.x, a.y);
-        *reinterpret_cast<uint32_t*>(&s.H[(r0 + 8) * LDT + col]) = pack_f16(b.x, b.y);
+        *reinterpret_cast<uint32_t*>(&s.H[0][swz<DVT>(r0, col)]) = pack_f16(a.x, a.y);
+        *reinterpret_cast<uint32_t*>(&s.H[0][swz<DVT>(r0 + 8, col)]) = pack_f16(b.x, b.y);
       }
   }
-  for (int i = 0; i < kStages - 1; ++i) issue(i);
+  __syncthreads();  // barriers initialised, H[0] written
 
-  for (int c = 0; c < n_chunks; ++c) {
-    typename S::Stage& b = s.st[c % kStages];
-    const long long slot = slot0 + c;
-    cp_async_wait<kStages - 2>();
-    __syncthreads();  // chunk c staged; s.H holds the state entering chunk c
-    issue(c + kStages - 1);
-
-    // publish the state entering the chunk for the output launch (fp16 tile)
-    {
-      __half* Hg = ws.H(slot, hv, p.Hv) + dvt * DK * DVT;
-      for (int i = tid; i < DK * (DVT / 8); i += kThreads) {
-        const int r = i / (DVT / 8), sg = i % (DVT / 8);
-        *reinterpret_cast<uint4*>(Hg + r * DVT + sg * 8) =
-            *reinterpret_cast<const uint4*>(&s.H[r * LDT + sg * 8]);
+  if (warp == 4) {
+    // ======================= producer ======================================
+    if (lane == 0) {
+      auto issue = [&](int c) {
+        typename S::Stage& b = s.st[c % kStages];
+        uint64_t* bar = &s.full[c % kStages];
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_g2s(b.W, ws.W(slot0 + c, hv, p.Hv), kC * DK * 2, bar);
+        bulk_g2s(b.Kt, ws.Kt(slot0 + c, hv, p.Hv), kC * DK * 2, bar);
+        bulk_g2s(b.U, ws.U(slot0 + c, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
+        bulk_g2s(b.gl, ws.gl(slot0 + c, hv, p.Hv), 16, bar);
+      };
+      for (int c = 0; c < kStages && c < n_chunks; ++c) issue(c);
+      for (int c = 0; c < n_chunks; ++c) {
+        const int hb = c & 1;
+        // publish the state entering chunk c and its V_new
+        if (!mbar_wait(&s.pub[hb], (c >> 1) & 1, p.err)) { s.abort = 1; break; }
+        bulk_s2g(ws.H(slot0 + c, hv, p.Hv) + dvt * DK * DVT, s.H[hb], DK * DVT * 2);
+        bulk_s2g(ws.Vn(slot0 + c, hv, p.Hv) + dvt * kC * DVT, s.Vn[hb], kC * DVT * 2);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&s.pubd[hb]);
+        // refill the stage chunk c used with chunk c + 3
+        if (c + kStages < n_chunks) {
+          if (!mbar_wait(&s.empty[c % kStages], (c / kStages) & 1, p.err)) { s.abort = 1; break; }
+          issue(c + kStages);
+        }
+        if (s.abort) break;
       }
+      bulk_wait<0>();
     }
+    return;
+  }
+
+  // ========================= chain (warps 0-3) ===============================
+  int c = 0;
+  for (; c < n_chunks; ++c) {
+    typename S::Stage& b = s.st[c % kStages];
+    const int hb = c & 1;
+    GDN_PHASE(16);  // loop top
+    if (!mbar_wait(&s.full[c % kStages], (c / kStages) & 1, p.err)) s.abort = 1;
+    GDN_PHASE(17);  // wait for staging
 
     // #5 read: V_new = U - W h   (warp: 16 token rows x the dv tile)
     const int r0 = 16 * warp + gq;
@@ -127,10 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
       for (int kk = 0; kk < DK; kk += 16) {
         uint32_t a[4], bb[4];
-        load_a(a, b.W, LDK, 16 * warp, kk, lane);
+        load_a_sw<DK>(a, b.W, 16 * warp, kk, lane);
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
-          load_b_kn(bb, s.H, LDT, 8 * j, kk, lane);
+          load_b_kn_sw<DVT>(bb, s.H[hb], 8 * j, kk, lane);
           mma_f16(wh[j], a, bb[0], bb[1]);
           mma_f16(wh[j + 1], a, bb[2], bb[3]);
         }
@@ -138,25 +165,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int col = 8 * j + 2 * tq;
-        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&b.U[r0 * LDT + col]));
+        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&b.U[r0 * DVT + col]));
         const float2 u1 =
-            __half22float2(*reinterpret_cast<const __half2*>(&b.U[(r0 + 8) * LDT + col]));
-        *reinterpret_cast<uint32_t*>(&s.Vn[r0 * LDT + col]) =
+            __half22float2(*reinterpret_cast<const __half2*>(&b.U[(r0 + 8) * DVT + col]));
+        *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0, col)]) =
             pack_f16(u0.x - wh[j][0], u0.y - wh[j][1]);
-        *reinterpret_cast<uint32_t*>(&s.Vn[(r0 + 8) * LDT + col]) =
+        *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0 + 8, col)]) =
             pack_f16(u1.x - wh[j][2], u1.y - wh[j][3]);
       }
     }
-    __syncthreads();  // V_new complete; every warp is done reading s.H
+    fence_proxy_async();
+    named_sync(1, kComputeThreads);  // V_new complete (H[hb] was complete before)
+    GDN_PHASE(20);  // V_new
+    if (s.abort) break;
+    if (tid == 0) mbar_arrive(&s.pub[hb]);
 
-    // publish V_new; #5 update: h = gamma_last h + Kt^T V_new
+    // #5 update: h = gamma_last h + Kt^T V_new
     {
-      __half* Vg = ws.Vn(slot, hv, p.Hv) + dvt * kC * DVT;
-      for (int i = tid; i < kC * (DVT / 8); i += kThreads) {
-        const int r = i / (DVT / 8), sg = i % (DVT / 8);
-        *reinterpret_cast<uint4*>(Vg + r * DVT + sg * 8) =
-            *reinterpret_cast<const uint4*>(&s.Vn[r * LDT + sg * 8]);
-      }
       const float gl = b.gl[0];
 #pragma unroll
       for (int mt = 0; mt < MTW; ++mt)
@@ -170,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
         uint32_t a[MTW][4];
 #pragma unroll
         for (int mt = 0; mt < MTW; ++mt)
-          load_a_trans(a[mt], b.Kt, LDK, 16 * (MTW * warp + mt), kk, lane);
+          load_a_trans_sw<DK>(a[mt], b.Kt, 16 * (MTW * warp + mt), kk, lane);
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
-          load_b_kn(bb, s.Vn, LDT, 8 * j, kk, lane);
+          load_b_kn_sw<DVT>(bb, s.Vn[hb], 8 * j, kk, lane);
 #pragma unroll
           for (int mt = 0; mt < MTW; ++mt) {
             mma_f16(hacc[mt][j], a[mt], bb[0], bb[1]);
@@ -181,21 +206,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
           }
         }
       }
-#pragma unroll
-      for (int mt = 0; mt < MTW; ++mt)
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int hr = 16 * (MTW * warp + mt) + gq, col = 8 * j + 2 * tq;
-          *reinterpret_cast<uint32_t*>(&s.H[hr * LDT + col]) =
-              pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
-          *reinterpret_cast<uint32_t*>(&s.H[(hr + 8) * LDT + col]) =
-              pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
-        }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[c % kStages]);  // this warp is done with the stage
+    GDN_PHASE(22);  // update
+    // H[hb ^ 1] held the state entering chunk c - 1: wait until its store has read it
+    if (c >= 1 && !mbar_wait(&s.pubd[hb ^ 1], ((c - 1) >> 1) & 1, p.err)) s.abort = 1;
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int hr = 16 * (MTW * warp + mt) + gq, col = 8 * j + 2 * tq;
+        *reinterpret_cast<uint32_t*>(&s.H[hb ^ 1][swz<DVT>(hr, col)]) =
+            pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
+        *reinterpret_cast<uint32_t*>(&s.H[hb ^ 1][swz<DVT>(hr + 8, col)]) =
+            pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
+      }
+    named_sync(1, kComputeThreads);  // next state copy complete
+    GDN_PHASE(23);  // state copy
   }
-  cp_async_wait<0>();
-
-  if (p.hT) {
+  if (tid == 0 && s.abort) {  // a wait gave up: let the copies already issued land
+    for (int cc = c + 1; cc < min(c + kStages, n_chunks); ++cc)
+      mbar_wait(&s.full[cc % kStages], (cc / kStages) & 1, nullptr);
+  }
+  if (p.hT && !s.abort) {
     float* hT = p.hT + ((long long)(n * p.Hv + hv) * DK) * p.dv + dvt * DVT;
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt)
@@ -210,22 +244,29 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
   }
 }
 
-template <int DK>
+template <int DK, int DVT>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
-  const size_t smem = sizeof(ChainSmem<DK>);
-  cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK>,
+  const size_t smem = sizeof(ChainSmem<DK, DVT>);
+  cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
-  gdn_chain_kernel<DK><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
+  gdn_chain_kernel<DK, DVT><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
   return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t launch_dk(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  if (ws.dvt == 16) return launch_t<DK, 16>(p, ws, stream);
+  if (ws.dvt == 32) return launch_t<DK, 32>(p, ws, stream);
+  return launch_t<DK, 64>(p, ws, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
-  if (p.dk == 128) return launch_t<128>(p, ws, stream);
-  return launch_t<64>(p, ws, stream);
+  if (p.dk == 128) return launch_dk<128>(p, ws, stream);
+  return launch_dk<64>(p, ws, stream);
 }
 
 }  // namespace gdn

@@ -12,6 +12,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Optional phase timing (compile with -DGDN_PROFILE): thread 0 of every CTA adds
+// the clock64() cycles spent since the previous mark to g_gdn_phase[id].  Off in
+// the library build, where the marks compile to nothing.
+#ifdef GDN_PROFILE
+extern __device__ unsigned long long g_gdn_phase[64];  // defined in gdn_abi.cu; needs -rdc
+#define GDN_PHASE_INIT long long gdn_phase_t = clock64()
+#define GDN_PHASE(id)                                                              \
+  do {                                                                             \
+    if (threadIdx.x == 0) {                                                        \
+      const long long now = clock64();                                             \
+      atomicAdd(&g_gdn_phase[(id)], (unsigned long long)(now - gdn_phase_t));      \
+      gdn_phase_t = now;                                                           \
+    }                                                                              \
+  } while (0)
+#else
+#define GDN_PHASE_INIT
+#define GDN_PHASE(id) \
+  do {                \
+  } while (0)
+#endif
+
 namespace gdn {
 
 // Device error word: bounded waits record why they gave up (read by gdn_device_status).
@@ -38,6 +59,98 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---- bulk copies (TMA engine, untiled) and mbarriers --------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// Arrive once and add `bytes` to the transaction count of the current phase.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Wait for phase `parity` of `bar` to complete, giving up after ~2^31 cycles
+// (about a second): returns false then, and records kErrWaitTimeout in *err.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned* err) {
+  const long long t0 = clock64();
+  unsigned done = 0;
+  while (true) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > (1ll << 31)) {
+      if (err) atomicExch(err, 1u);
+      return false;
+    }
+  }
+}
+// global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned;
+// completion is counted on `bar` (its transaction count must expect the bytes).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, unsigned bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// shared -> global, same size and alignment rules; tracked by bulk_commit/bulk_wait.
+__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gmem_dst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until at most N committed bulk stores still read their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy / tensor core) reads.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// ---- swizzled 16-bit tiles ---------------------------------------------------
+// Dense row-major tiles whose 16-byte chunks are XOR-permuted so that 8
+// consecutive rows read at one column chunk hit 8 different bank groups
+// (ldmatrix without padding, and the layout survives a verbatim bulk copy).
+//   W = 64 or 128 halves per row: chunk c of row r sits at chunk
+//       (c & ~7) | ((c ^ r) & 7)          (XOR inside each 128-byte segment)
+//   W = 32 halves per row (64-byte rows): chunk c sits at c ^ ((r >> 1) & 3)
+//   W = 16 halves per row (32-byte rows): chunk c sits at c ^ ((r >> 2) & 1)
+template <int W>
+__device__ __forceinline__ int swz(int r, int col) {
+  static_assert(W == 16 || W == 32 || W == 64 || W == 128, "tile width");
+  const int c = col >> 3;
+  int pc;
+  if (W == 16) pc = c ^ ((r >> 2) & 1);
+  else if (W == 32) pc = c ^ ((r >> 1) & 3);
+  else pc = (c & ~7) | ((c ^ r) & 7);
+  return r * W + (pc << 3) + (col & 7);
+}
+
+// mbarrier arrive (release), one count.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier among the first `nthreads` threads of the block (id 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---- ldmatrix ---------------------------------------------------------------
@@ -97,6 +210,27 @@ __device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __half* base, 
   const int kr = k0 + (lane & 7) + ((g & 1) << 3);
   const int nc = n0 + ((g >> 1) << 3);
   ldsm_x4_t(b[0], b[1], b[2], b[3], base + kr * ld + nc);
+}
+
+// Swizzled-tile variants of the fragment loads (tile width W halves, see swz).
+template <int W>
+__device__ __forceinline__ void load_a_sw(uint32_t (&a)[4], const __half* base, int m0, int k0,
+                                          int lane) {
+  ldsm_x4(a[0], a[1], a[2], a[3], base + swz<W>(m0 + (lane & 15), k0 + ((lane >> 4) << 3)));
+}
+template <int W>
+__device__ __forceinline__ void load_a_trans_sw(uint32_t (&a)[4], const __half* base, int m0,
+                                                int k0, int lane) {
+  const int g = lane >> 3;
+  ldsm_x4_t(a[0], a[1], a[2], a[3],
+            base + swz<W>(k0 + (lane & 7) + ((g >> 1) << 3), m0 + ((g & 1) << 3)));
+}
+template <int W>
+__device__ __forceinline__ void load_b_kn_sw(uint32_t (&b)[4], const __half* base, int n0, int k0,
+                                             int lane) {
+  const int g = lane >> 3;
+  ldsm_x4_t(b[0], b[1], b[2], b[3],
+            base + swz<W>(k0 + (lane & 7) + ((g & 1) << 3), n0 + ((g >> 1) << 3)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

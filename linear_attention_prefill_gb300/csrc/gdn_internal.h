@@ -22,6 +22,7 @@ struct FwdParams {
   int T;              // tokens per row (packed total with cu_seqlens)
   int Hqk, Hv, dk, dv, chunk;
   float scale;
+  unsigned* err;      // device error word: bounded waits record a timeout here
 };
 
 // One decode step.
@@ -38,24 +39,28 @@ struct StepParams {
 };
 
 // Workspace of the bf16 forward: one record per (chunk slot, v head), all fp16
-// row-major unless stated:
+// row-major with 16-byte chunks XOR-swizzled per row (gdn::swz<width>), so a
+// verbatim bulk copy lands in shared memory ready for conflict-free ldmatrix:
 //   W    [64][dk]         Tm diag(beta gamma) K                  (gdn_prep)
 //   Kt   [64][dk]         diag(e) K, e_j = exp(G_last - G_j)     (gdn_prep)
 //   Qt   [64][dk]         diag(scale gamma) Q                    (gdn_prep)
 //   P    [64][64]         tril(scale exp(G_i - G_j) q_i.k_j)     (gdn_prep)
-//   U    [dv/32][64][32]  Tm diag(beta) V, one block per 32-column dv tile (gdn_prep)
+//   U    [dv/t][64][t]    Tm diag(beta) V, one block per t-column dv tile, not swizzled
 //   gl   fp32 + pad       gamma_last = exp(G_last)               (gdn_prep)
-//   H    [dv/32][dk][32]  state entering the chunk, per dv tile  (gdn_chain)
-//   Vn   [dv/32][64][32]  V_new = U - W h, per dv tile           (gdn_chain)
+//   H    [dv/t][dk][t]    state entering the chunk, per dv tile  (gdn_chain)
+//   Vn   [dv/t][64][t]    V_new = U - W h, per dv tile           (gdn_chain)
+// The dv tile t (16, 32 or 64 columns, one chain CTA each) is picked per call
+// by dv_tile(): the narrowest that still leaves at most ~one CTA per SM, since
+// every chain CTA must take in the whole W and Kt of its chain.
 // gdn_out reads Qt, P, H and Vn.  Sequence n's chunk c lives in slot
 // first_slot(n) + c: n * ceil(T / 64) for fixed-length rows; floor(cu[n] / 64) +
 // n with cu_seqlens, which never overlaps because floor((a + L) / 64) -
 // floor(a / 64) + 1 >= ceil(L / 64), and ends below floor(T / 64) + N + 1.
 constexpr int kChunk = 64;
-constexpr int kDvTile = 32;  // dv columns per chain CTA
 
 struct WsLayout {
   char* base;
+  int dvt;                  // dv tile width of the chain launch
   long long n_slots;        // chunk slots per v head
   long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
   long long task_bytes, kt_off, qt_off, p_off, u_off, gl_off, h_off, vn_off;
@@ -93,10 +98,20 @@ struct WsLayout {
   }
 };
 
+// dv tile of the chain launch: 16 columns while chains x dv/16 CTAs fit on the
+// 152 SMs, else 32, else 64 (and never wider than dv).
+inline int dv_tile(const FwdParams& p) {
+  const long long chains = (long long)p.N * p.Hv;
+  if (chains * (p.dv / 16) <= 152) return 16;
+  if (chains * (p.dv / 32) <= 152 || p.dv == 32) return 32;
+  return 64;
+}
+
 // Layout for one call (sizes validated); base may be null when only sizing.
 inline WsLayout ws_layout(const FwdParams& p, void* base) {
   WsLayout w;
   w.base = static_cast<char*>(base);
+  w.dvt = dv_tile(p);
   if (p.cu_seqlens) {
     w.slots_per_seq = 0;
     w.n_slots = (long long)p.T / kChunk + p.N + 1;

@@ -3,7 +3,8 @@
 //   O = diag(scale gamma) Q h + P V_new   = Qt h + P V_new
 // with h the state entering the chunk and V_new = U - W h, both published by
 // gdn_chain.  Every (chunk, v head) is independent once the chain has passed
-// it, so this launch is chunk-parallel over the whole GPU.  Products on fp16
+// it, so this launch is chunk-parallel over the whole GPU.  One thread stages
+// the record with bulk copies (swizzled tiles, see gdn::swz); products on fp16
 // tensor cores (mma.sync) with fp32 accumulation; o is rounded once to bf16.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -14,25 +15,25 @@ namespace {
 constexpr int kC = 64;
 constexpr int kThreads = 256;
 
-template <int DK, int DV>
+template <int DK, int DV, int T32>
 struct OutSmem {
-  static constexpr int LDK = DK + 8;
-  static constexpr int LDV = DV + 8;
-  static constexpr int LDC = kC + 8;
+  static constexpr int LDO = DV + 8;
   union {
-    __half Qt[kC * LDK];
-    __nv_bfloat16 O[kC * LDV];  // output staging once the products are done
+    __half Qt[kC * DK];             // swz<DK>
+    __nv_bfloat16 O[kC * LDO];      // output staging once the products are done
   };
-  __half P[kC * LDC];
-  __half H[DK * LDV];
-  __half Vn[kC * LDV];
+  __half P[kC * kC];                // swz<64>
+  __half H[DV / T32][DK * T32];     // swz<32> per dv tile
+  __half Vn[DV / T32][kC * T32];    // swz<32> per dv tile
+  uint64_t full;
+  int abort;
 };
 
-template <int DK, int DV>
+template <int DK, int DV, int T32>
 __global__ void __launch_bounds__(kThreads, 2) gdn_out_kernel(const FwdParams p, WsLayout ws) {
-  using S = OutSmem<DK, DV>;
-  constexpr int LDK = S::LDK, LDV = S::LDV, LDC = S::LDC;
-  constexpr int T32 = kDvTile;
+  using S = OutSmem<DK, DV, T32>;
+  constexpr int LDO = S::LDO;
+  constexpr unsigned kBytes = kC * DK * 2 + kC * kC * 2 + DK * DV * 2 + kC * DV * 2;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -48,33 +49,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_out_kernel(const FwdParams p,
   const long long t0 = t_seq + (long long)c * kC;
   const int L = (int)min((long long)kC, len - (long long)c * kC);
 
-  {
-    const __half* Qg = ws.Qt(slot, hv, p.Hv);
-    const __half* Pg = ws.P(slot, hv, p.Hv);
-    const __half* Hg = ws.H(slot, hv, p.Hv);
-    const __half* Vg = ws.Vn(slot, hv, p.Hv);
-    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-      const int r = i / (DK / 8), sg = i % (DK / 8);
-      cp_async16(&s.Qt[r * LDK + sg * 8], Qg + r * DK + sg * 8, true);
-    }
-    for (int i = tid; i < kC * (kC / 8); i += kThreads) {
-      const int r = i / (kC / 8), sg = i % (kC / 8);
-      cp_async16(&s.P[r * LDC + sg * 8], Pg + r * kC + sg * 8, true);
-    }
-    for (int i = tid; i < DK * (DV / 8); i += kThreads) {  // [dv/32][dk][32] -> [dk][dv]
-      const int r = i / (DV / 8), col = (i % (DV / 8)) * 8;
-      const int t = col / T32, w = col % T32;
-      cp_async16(&s.H[r * LDV + col], Hg + (t * DK + r) * T32 + w, true);
-    }
-    for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // [dv/32][64][32] -> [64][dv]
-      const int r = i / (DV / 8), col = (i % (DV / 8)) * 8;
-      const int t = col / T32, w = col % T32;
-      cp_async16(&s.Vn[r * LDV + col], Vg + (t * kC + r) * T32 + w, true);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
+  if (tid == 0) {
+    s.abort = 0;
+    mbar_init(&s.full, 1);
+    mbar_fence_init();
+    mbar_expect_tx(&s.full, kBytes);
+    bulk_g2s(s.Qt, ws.Qt(slot, hv, p.Hv), kC * DK * 2, &s.full);
+    bulk_g2s(s.P, ws.P(slot, hv, p.Hv), kC * kC * 2, &s.full);
+    bulk_g2s(s.H[0], ws.H(slot, hv, p.Hv), DK * DV * 2, &s.full);
+    bulk_g2s(s.Vn[0], ws.Vn(slot, hv, p.Hv), kC * DV * 2, &s.full);
   }
-  __syncthreads();
+  __syncthreads();  // the barrier is initialised before anyone waits on it
+  if (!mbar_wait(&s.full, 0, p.err)) s.abort = 1;
 
   const int rb = warp & 3, nh = warp >> 2;
   constexpr int NT = DV / 16;  // n8 tiles per warp (half the columns)
@@ -86,31 +72,34 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_out_kernel(const FwdParams p,
 #pragma unroll 2
   for (int kk = 0; kk < DK; kk += 16) {
     uint32_t a[4], b[4];
-    load_a(a, s.Qt, LDK, 16 * rb, kk, lane);
+    load_a_sw<DK>(a, s.Qt, 16 * rb, kk, lane);
 #pragma unroll
     for (int j = 0; j < NT; j += 2) {
-      load_b_kn(b, s.H, LDV, nh * (DV / 2) + 8 * j, kk, lane);
+      const int n0 = nh * (DV / 2) + 8 * j;
+      load_b_kn_sw<T32>(b, s.H[n0 / T32], n0 % T32, kk, lane);
       mma_f16(acc[j], a, b[0], b[1]);
       mma_f16(acc[j + 1], a, b[2], b[3]);
     }
   }
   for (int kk = 0; kk <= 16 * rb; kk += 16) {  // P is lower triangular
     uint32_t a[4], b[4];
-    load_a(a, s.P, LDC, 16 * rb, kk, lane);
+    load_a_sw<kC>(a, s.P, 16 * rb, kk, lane);
 #pragma unroll
     for (int j = 0; j < NT; j += 2) {
-      load_b_kn(b, s.Vn, LDV, nh * (DV / 2) + 8 * j, kk, lane);
+      const int n0 = nh * (DV / 2) + 8 * j;
+      load_b_kn_sw<T32>(b, s.Vn[n0 / T32], n0 % T32, kk, lane);
       mma_f16(acc[j], a, b[0], b[1]);
       mma_f16(acc[j + 1], a, b[2], b[3]);
     }
   }
   __syncthreads();  // Qt is dead: stage O in its place
+  if (s.abort) return;
   const int r0 = 16 * rb + gq;
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     const int col = nh * (DV / 2) + 8 * j + 2 * tq;
-    *reinterpret_cast<uint32_t*>(&s.O[r0 * LDV + col]) = pack_bf16(acc[j][0], acc[j][1]);
-    *reinterpret_cast<uint32_t*>(&s.O[(r0 + 8) * LDV + col]) = pack_bf16(acc[j][2], acc[j][3]);
+    *reinterpret_cast<uint32_t*>(&s.O[r0 * LDO + col]) = pack_bf16(acc[j][0], acc[j][1]);
+    *reinterpret_cast<uint32_t*>(&s.O[(r0 + 8) * LDO + col]) = pack_bf16(acc[j][2], acc[j][3]);
   }
   __syncthreads();
   const long long v_tok = (long long)p.Hv * DV;
@@ -118,30 +107,37 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_out_kernel(const FwdParams p,
   for (int i = tid; i < L * (DV / 8); i += kThreads) {
     const int r = i / (DV / 8), sg = i % (DV / 8);
     *reinterpret_cast<uint4*>(og + (t0 + r) * v_tok + sg * 8) =
-        *reinterpret_cast<const uint4*>(&s.O[r * LDV + sg * 8]);
+        *reinterpret_cast<const uint4*>(&s.O[r * LDO + sg * 8]);
   }
 }
 
-template <int DK, int DV>
+template <int DK, int DV, int T>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
-  const size_t smem = sizeof(OutSmem<DK, DV>);
-  cudaError_t e = cudaFuncSetAttribute(gdn_out_kernel<DK, DV>,
+  const size_t smem = sizeof(OutSmem<DK, DV, T>);
+  cudaError_t e = cudaFuncSetAttribute(gdn_out_kernel<DK, DV, T>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const long long grid = ws.n_slots * p.Hv;
-  gdn_out_kernel<DK, DV><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
+  gdn_out_kernel<DK, DV, T><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
   return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t launch_dv(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  if (ws.dvt == 16) return launch_t<DK, DV, 16>(p, ws, stream);
+  if (ws.dvt == 32) return launch_t<DK, DV, 32>(p, ws, stream);
+  return launch_t<DK, DV, 64>(p, ws, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
   if (p.dk == 128) {
-    if (p.dv == 128) return launch_t<128, 128>(p, ws, stream);
-    return launch_t<128, 64>(p, ws, stream);
+    if (p.dv == 128) return launch_dv<128, 128>(p, ws, stream);
+    return launch_dv<128, 64>(p, ws, stream);
   }
-  if (p.dv == 128) return launch_t<64, 128>(p, ws, stream);
-  return launch_t<64, 64>(p, ws, stream);
+  if (p.dv == 128) return launch_dv<64, 128>(p, ws, stream);
+  return launch_dv<64, 64>(p, ws, stream);
 }
 
 }  // namespace gdn

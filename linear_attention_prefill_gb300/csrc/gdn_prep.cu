@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
+  GDN_PHASE_INIT;
   // task -> (chunk slot, v head) -> (sequence, chunk within it)
   const int hv = blockIdx.x % p.Hv;
   const long long slot = blockIdx.x / p.Hv;
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
     cp_async_wait<0>();
   }
   __syncthreads();
+  GDN_PHASE(0);  // staging
   for (int i = tid; i < kC * (DK / 8); i += kThreads) {
     const int r = i / (DK / 8), sg = i % (DK / 8);
     bf16x8_to_f16x8(&s.K[r * LDK + sg * 8]);
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
     if (lane == 31) *ws.gl(slot, hv, p.Hv) = expf(Glast);
   }
   __syncthreads();
+  GDN_PHASE(1);  // convert + gate
 
   // ---- #2 KKT and QK^T grams (lower triangle) -------------------------------
   __half* Pout = ws.P(slot, hv, p.Hv);
@@ -171,16 +174,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
         }
       }
     }
+    GDN_PHASE(2);  // grams
     // the scaled copies Qt = diag(scale gamma) Q and Kt = diag(e) K
     __half* Qt = ws.Qt(slot, hv, p.Hv);
     __half* Kt = ws.Kt(slot, hv, p.Hv);
     for (int i = tid; i < kC * (DK / 8); i += kThreads) {
       const int r = i / (DK / 8), sg = i % (DK / 8);
-      *reinterpret_cast<uint4*>(Qt + r * DK + sg * 8) =
+      *reinterpret_cast<uint4*>(Qt + swz<DK>(r, sg * 8)) =
           scale_f16x8(&s.Q[r * LDK + sg * 8], p.scale * s.gam[r]);
-      *reinterpret_cast<uint4*>(Kt + r * DK + sg * 8) = scale_f16x8(&s.K[r * LDK + sg * 8], s.e[r]);
+      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, sg * 8)) = scale_f16x8(&s.K[r * LDK + sg * 8], s.e[r]);
     }
     __syncthreads();  // Q is dead: its storage becomes A
+    GDN_PHASE(3);  // Qt, Kt
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
 #pragma unroll
@@ -198,14 +203,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
           s.A[r * LDA + cc] = av[y];
         }
         *reinterpret_cast<uint32_t*>(&s.Ah[r * LDC + c0]) = pack_f16(av[0], av[1]);
-        *reinterpret_cast<uint32_t*>(Pout + r * kC + c0) = pack_f16(pv[0], pv[1]);
+        *reinterpret_cast<uint32_t*>(Pout + swz<kC>(r, c0)) = pack_f16(pv[0], pv[1]);
       }
     }
   }
   __syncthreads();
 
+  GDN_PHASE(4);  // masks
   // ---- #3 Solve and the scaled fp16 operands --------------------------------
   solve_unit_lower_64(s.A, LDA, s.Ah, s.Tm, LDA, s.Th, LDC);
+  GDN_PHASE(5);  // solve
   for (int e = tid; e < kC * kC; e += kThreads) {
     const int r = e >> 6, cc = e & 63;
     const float tv = s.Tm[r * LDA + cc];
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
     s.Tu[r * LDC + cc] = __float2half_rn(tv * b);
   }
   __syncthreads();
+  GDN_PHASE(6);  // Tw, Tu
 
   // ---- #4 W = Tw K, U = Tu V (lower-triangular Tw/Tu: k <= row block) -------
   {
@@ -261,19 +269,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
     }
   }
   __syncthreads();
+  GDN_PHASE(7);  // W/U products
   __half* Wout = ws.W(slot, hv, p.Hv);
   __half* Uout = ws.U(slot, hv, p.Hv);
   for (int i = tid; i < kC * (DK / 8); i += kThreads) {
     const int r = i / (DK / 8), sg = i % (DK / 8);
-    *reinterpret_cast<uint4*>(Wout + r * DK + sg * 8) =
+    *reinterpret_cast<uint4*>(Wout + swz<DK>(r, sg * 8)) =
         *reinterpret_cast<const uint4*>(&s.Wst[r * LDK + sg * 8]);
   }
-  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // U tile-major: [dv/32][64][32]
+  const int dvt = ws.dvt;
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // U tile-major: [dv/t][64][t]
     const int r = i / (DV / 8), sg = i % (DV / 8);
-    const int col = sg * 8, t = col / kDvTile, w = col % kDvTile;
-    *reinterpret_cast<uint4*>(Uout + (t * kC + r) * kDvTile + w) =
+    const int col = sg * 8, t = col / dvt, w = col % dvt;
+    *reinterpret_cast<uint4*>(Uout + (t * kC + r) * dvt + w) =
         *reinterpret_cast<const uint4*>(&s.Ust[r * LDV + col]);
   }
+  GDN_PHASE(8);  // W/U stores
 }
 
 template <int DK, int DV>
