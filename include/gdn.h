@@ -106,6 +106,33 @@ gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const f
                             const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
                             gdn_stream_t stream);
 
+/*
+ * gdn_chunk_fwd_noalloc - gdn_chunk_fwd for callers that must not allocate
+ * device memory: it runs on a workspace of 32 MiB compiled into the library
+ * (a static device array) and makes no allocation call of any kind.  No
+ * passage of the pages corresponds to it; it exists for callers such as a
+ * serving loop that may not take an allocator's locks or risk the device
+ * synchronisation an allocation can imply, or code embedded in a runtime that
+ * owns all device memory through its own pool.
+ *  - Limit: gdn_chunk_fwd_workspace_size(...) must be at most 32 MiB (about
+ *    270 chunk-and-v-head records at dk = dv = 128, e.g. 4096 tokens x 4 v
+ *    heads); larger sizes return GDN_ERR_INVALID_ARG and launch nothing.
+ *  - Every GPU that runs the library's device code keeps those 32 MiB until
+ *    the process exits.
+ *  - The first call on each device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and its contents persist between calls;
+ *    each call rewrites every byte it later reads, so nothing needs clearing,
+ *    but calls that overlap on the GPU (different streams, or different host
+ *    threads without ordering) race on it.
+ * Arguments, results and other errors are those of gdn_chunk_fwd.
+ */
+gdn_status gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* h0, void* o, float* hT, int B,
+                                 int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                                 const int32_t* cu_seqlens, gdn_stream_t stream);
+
 /* gdn_chunk_fwd_f32 - as gdn_chunk_fwd with fp32 q, k, v and o (fp32 throughout).
  * One fused launch per call; no workspace. */
 gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,

@@ -28,6 +28,7 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "gdn_chunk_fwd": (_I, _FWD_ARGS),
     "gdn_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "gdn_chunk_fwd_noalloc": (_I, _FWD_ARGS),
     "gdn_chunk_fwd_workspace_size": (_SZ, [_I] * 8),
     "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
     "gdn_recurrent_step": (_I, _STEP_ARGS),

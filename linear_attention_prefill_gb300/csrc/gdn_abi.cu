@@ -6,6 +6,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -245,6 +247,55 @@ gdn_status gdn_device_status(gdn_stream_t stream) {
     return fail(GDN_ERR_TIMEOUT, "a bounded device-side wait gave up");
   if (word != 0u) return fail(GDN_ERR_TIMEOUT, "device error word 0x%x", word);
   return GDN_OK;
+}
+
+}  // extern "C"
+
+// ---- forward without any allocation ------------------------------------------
+// A fixed workspace compiled into the library: the device keeps these bytes
+// from the moment the library's device code is first used until the process
+// exits, on every GPU it runs on.  Host code must not use the array's name as a
+// device address; the address is looked up once per device below.
+namespace {
+constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[64] = {};  // per device ordinal, filled on first use
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* h0, void* o, float* hT, int B,
+                                 int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                                 const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  const size_t need = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+  if (need > kNoAllocWorkspaceBytes)
+    return fail(GDN_ERR_INVALID_ARG,
+                "these sizes need %zu bytes of workspace; the built-in workspace holds %zu "
+                "(use gdn_chunk_fwd_ex with a caller buffer)",
+                need, kNoAllocWorkspaceBytes);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "querying the current device");
+  if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_address[dev]) {
+      e = cudaGetSymbolAddress(&g_noalloc_address[dev], g_noalloc_workspace);
+      if (e != cudaSuccess) {
+        g_noalloc_address[dev] = nullptr;
+        return cuda_fail(e, "locating the built-in workspace");
+      }
+    }
+    ws = g_noalloc_address[dev];
+  }
+  return run_fwd_bf16(p, ws, kNoAllocWorkspaceBytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gdn_status_string(gdn_status s) {
