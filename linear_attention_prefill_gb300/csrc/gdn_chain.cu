@@ -25,6 +25,7 @@ constexpr int kC = 64;
 constexpr int kComputeThreads = 128;  // warps 0-3
 constexpr int kThreads = 160;         // + producer warp
 constexpr int kStages = 3;
+constexpr int kPub = 3;  // H / V_new buffers: the store of chunk c - 1 has a whole step to finish
 
 template <int DK, int DVT>
 struct ChainSmem {
@@ -35,12 +36,12 @@ struct ChainSmem {
     float gl[4];
   };
   Stage st[kStages];
-  __half H[2][DK * DVT];   // swz<DVT>: state entering the chunk (double-buffered for the store)
-  __half Vn[2][kC * DVT];  // swz<DVT>
-  uint64_t full[kStages];  // producer -> chain: chunk staged (transaction bytes)
-  uint64_t empty[kStages]; // chain -> producer: stage consumed (4 warp arrivals)
-  uint64_t pub[2];         // chain -> producer: H[b], Vn[b] ready to store
-  uint64_t pubd[2];        // producer -> chain: H[b], Vn[b] read by the store
+  __half H[kPub][DK * DVT];   // swz<DVT>: state entering the chunk (ring for the stores)
+  __half Vn[kPub][kC * DVT];  // swz<DVT>
+  uint64_t full[kStages];     // producer -> chain: chunk staged (transaction bytes)
+  uint64_t empty[kStages];    // chain -> producer: stage consumed (4 warp arrivals)
+  uint64_t pub[kPub];         // chain -> producer: H[b], Vn[b] ready to store
+  uint64_t pubd[kPub];        // producer -> chain: H[b], Vn[b] read by the store
   int abort;
 };
 
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPub; ++i) {
       mbar_init(&s.pub[i], 1);
       mbar_init(&s.pubd[i], 1);
     }
@@ -114,9 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
       };
       for (int c = 0; c < kStages && c < n_chunks; ++c) issue(c);
       for (int c = 0; c < n_chunks; ++c) {
-        const int hb = c & 1;
+        const int hb = c % kPub;
         // publish the state entering chunk c and its V_new
-        if (!mbar_wait(&s.pub[hb], (c >> 1) & 1, p.err)) { s.abort = 1; break; }
+        if (!mbar_wait(&s.pub[hb], (c / kPub) & 1, p.err)) { s.abort = 1; break; }
         bulk_s2g(ws.H(slot0 + c, hv, p.Hv) + dvt * DK * DVT, s.H[hb], DK * DVT * 2);
         bulk_s2g(ws.Vn(slot0 + c, hv, p.Hv) + dvt * kC * DVT, s.Vn[hb], kC * DVT * 2);
         bulk_commit();
@@ -135,31 +136,48 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
   }
 
   // ========================= chain (warps 0-3) ===============================
+  // Per chunk: V_new (depth-4 accumulation chains: K split in two halves), one
+  // barrier, the state update straight into the next H buffer, one barrier.
+  // The A fragments of W and Kt are read before the state they multiply is ready.
   int c = 0;
   for (; c < n_chunks; ++c) {
     typename S::Stage& b = s.st[c % kStages];
-    const int hb = c & 1;
+    const int hb = c % kPub, hn = (c + 1) % kPub;
     GDN_PHASE(16);  // loop top
     if (!mbar_wait(&s.full[c % kStages], (c / kStages) & 1, p.err)) s.abort = 1;
     GDN_PHASE(17);  // wait for staging
+    uint32_t wa[DK / 16][4];  // W rows of this warp, all k steps
+#pragma unroll
+    for (int ks = 0; ks < DK / 16; ++ks) load_a_sw<DK>(wa[ks], b.W, 16 * warp, 16 * ks, lane);
+    uint32_t ka[kC / 16][MTW][4];  // Kt^T rows of this warp, all k steps
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks)
+#pragma unroll
+      for (int mt = 0; mt < MTW; ++mt)
+        load_a_trans_sw<DK>(ka[ks][mt], b.Kt, 16 * (MTW * warp + mt), 16 * ks, lane);
 
     // #5 read: V_new = U - W h   (warp: 16 token rows x the dv tile)
     const int r0 = 16 * warp + gq;
     {
-      float wh[NT][4];
+      float wh[2][NT][4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
+      for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) wh[j][x] = 0.f;
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int kk = 0; kk < DK; kk += 16) {
-        uint32_t a[4], bb[4];
-        load_a_sw<DK>(a, b.W, 16 * warp, kk, lane);
+          for (int x = 0; x < 4; ++x) wh[hh][j][x] = 0.f;
 #pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-          load_b_kn_sw<DVT>(bb, s.H[hb], 8 * j, kk, lane);
-          mma_f16(wh[j], a, bb[0], bb[1]);
-          mma_f16(wh[j + 1], a, bb[2], bb[3]);
+      for (int ks = 0; ks < DK / 32; ++ks) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int kk = 16 * (ks + hh * (DK / 32));
+#pragma unroll
+          for (int j = 0; j < NT; j += 2) {
+            uint32_t bb[4];
+            load_b_kn_sw<DVT>(bb, s.H[hb], 8 * j, kk, lane);
+            mma_f16(wh[hh][j], wa[kk / 16], bb[0], bb[1]);
+            mma_f16(wh[hh][j + 1], wa[kk / 16], bb[2], bb[3]);
+          }
         }
       }
 #pragma unroll
@@ -169,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
         const float2 u1 =
             __half22float2(*reinterpret_cast<const __half2*>(&b.U[(r0 + 8) * DVT + col]));
         *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0, col)]) =
-            pack_f16(u0.x - wh[j][0], u0.y - wh[j][1]);
+            pack_f16(u0.x - wh[0][j][0] - wh[1][j][0], u0.y - wh[0][j][1] - wh[1][j][1]);
         *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0 + 8, col)]) =
-            pack_f16(u1.x - wh[j][2], u1.y - wh[j][3]);
+            pack_f16(u1.x - wh[0][j][2] - wh[1][j][2], u1.y - wh[0][j][3] - wh[1][j][3]);
       }
     }
     fence_proxy_async();
@@ -180,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
     if (s.abort) break;
     if (tid == 0) mbar_arrive(&s.pub[hb]);
 
-    // #5 update: h = gamma_last h + Kt^T V_new
+    // #5 update: h = gamma_last h + Kt^T V_new, written straight into H[hn]
     {
       const float gl = b.gl[0];
 #pragma unroll
@@ -190,19 +208,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
           for (int x = 0; x < 4; ++x) hacc[mt][j][x] *= gl;
 #pragma unroll
-      for (int kk = 0; kk < kC; kk += 16) {
-        uint32_t bb[4];
-        uint32_t a[MTW][4];
-#pragma unroll
-        for (int mt = 0; mt < MTW; ++mt)
-          load_a_trans_sw<DK>(a[mt], b.Kt, 16 * (MTW * warp + mt), kk, lane);
+      for (int ks = 0; ks < kC / 16; ++ks) {
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
-          load_b_kn_sw<DVT>(bb, s.Vn[hb], 8 * j, kk, lane);
+          uint32_t bb[4];
+          load_b_kn_sw<DVT>(bb, s.Vn[hb], 8 * j, 16 * ks, lane);
 #pragma unroll
           for (int mt = 0; mt < MTW; ++mt) {
-            mma_f16(hacc[mt][j], a[mt], bb[0], bb[1]);
-            mma_f16(hacc[mt][j + 1], a[mt], bb[2], bb[3]);
+            mma_f16(hacc[mt][j], ka[ks][mt], bb[0], bb[1]);
+            mma_f16(hacc[mt][j + 1], ka[ks][mt], bb[2], bb[3]);
           }
         }
       }
@@ -210,16 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[c % kStages]);  // this warp is done with the stage
     GDN_PHASE(22);  // update
-    // H[hb ^ 1] held the state entering chunk c - 1: wait until its store has read it
-    if (c >= 1 && !mbar_wait(&s.pubd[hb ^ 1], ((c - 1) >> 1) & 1, p.err)) s.abort = 1;
+    // H[hn] last held the state entering chunk c - 2: its store must have read it
+    if (c >= 2 && !mbar_wait(&s.pubd[hn], ((c - 2) / kPub) & 1, p.err)) s.abort = 1;
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int hr = 16 * (MTW * warp + mt) + gq, col = 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&s.H[hb ^ 1][swz<DVT>(hr, col)]) =
+        *reinterpret_cast<uint32_t*>(&s.H[hn][swz<DVT>(hr, col)]) =
             pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
-        *reinterpret_cast<uint32_t*>(&s.H[hb ^ 1][swz<DVT>(hr + 8, col)]) =
+        *reinterpret_cast<uint32_t*>(&s.H[hn][swz<DVT>(hr + 8, col)]) =
             pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
       }
     named_sync(1, kComputeThreads);  // next state copy complete

@@ -13,8 +13,11 @@
 // inter-chunk term).  The serial Reduce (#5) runs in gdn_chain.cu, the final
 // Map (#6) in gdn_out.cu; both read this kernel's workspace records.
 //
-// Tensor-core products use fp16 operands with fp32 accumulation (q, k, v are
-// staged as bf16 and rewritten in place as fp16, exact in fp16's normal range).
+// Tensor-core products accumulate in fp32.  The grams and W = (Tm diag(beta
+// gamma)) K take the bf16 inputs as they are (W's left factor rounded to bf16:
+// its share of the error is below 1e-3 of RMS); U = Tm diag(beta) V takes fp16
+// operands (v rewritten in place, exact in fp16's normal range), since U's
+// rounding feeds V_new and the output directly.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -30,8 +33,8 @@ struct PrepSmem {
   static constexpr int LDV = DV + 8;
   static constexpr int LDC = kC + 8;
   static constexpr int LDA = kC + 4;   // fp32 row stride of A and Tm
-  __half K[kC * LDK];
-  union {                              // Q until the grams are done, then A, then U staging
+  __half K[kC * LDK];                  // bf16 bits (grams and W take bf16 operands)
+  union {                              // Q (bf16 bits) until the grams are done, then A, then U staging
     __half Q[kC * LDK];
     float A[kC * LDA];
     __half Ust[kC * LDV];
@@ -43,20 +46,23 @@ struct PrepSmem {
   };
   __half Ah[kC * LDC];
   __half Th[kC * LDC];
-  __half Tw[kC * LDC];
+  union {                              // P staging for its bulk store, then Tw (bf16 bits)
+    __half Pst[kC * kC];
+    __half Tw[kC * LDC];
+  };
   __half Tu[kC * LDC];
   float g[kC], beta[kC], G[kC], gam[kC], e[kC];
 };
 
-// 8 fp16 values at p (16-byte aligned) times `scale`, rounded once.
-__device__ __forceinline__ uint4 scale_f16x8(const __half* p, float scale) {
+// 8 bf16 values at p (16-byte aligned) times `scale`, rounded once to fp16.
+__device__ __forceinline__ uint4 scale_bf16x8_to_f16(const __half* p, float scale) {
   uint4 raw = *reinterpret_cast<const uint4*>(p);
-  const __half2* h = reinterpret_cast<const __half2*>(&raw);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
   uint4 out;
   __half2* o = reinterpret_cast<__half2*>(&out);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(h[i]);
+    const float2 f = __bfloat1622float2(h[i]);
     o[i] = __floats2half2_rn(f.x * scale, f.y * scale);
   }
   return out;
@@ -114,12 +120,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
   }
   __syncthreads();
   GDN_PHASE(0);  // staging
-  for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-    const int r = i / (DK / 8), sg = i % (DK / 8);
-    bf16x8_to_f16x8(&s.K[r * LDK + sg * 8]);
-    bf16x8_to_f16x8(&s.Q[r * LDK + sg * 8]);
-  }
-  for (int i = tid; i < kC * (DV / 8); i += kThreads) {
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // V -> fp16 (U takes fp16 operands)
     const int r = i / (DV / 8), sg = i % (DV / 8);
     bf16x8_to_f16x8(&s.V[r * LDV + sg * 8]);
   }
@@ -161,16 +162,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
         load_a(ak, s.K, LDK, 16 * rb, kk, lane);
         load_a(aq, s.Q, LDK, 16 * rb, kk, lane);
         load_b_nk(b, s.K, LDK, 32 * ch, kk, lane);
-        mma_f16(aK[0], ak, b[0], b[1]);
-        mma_f16(aK[1], ak, b[2], b[3]);
-        mma_f16(aQ[0], aq, b[0], b[1]);
-        mma_f16(aQ[1], aq, b[2], b[3]);
+        mma_bf16(aK[0], ak, b[0], b[1]);
+        mma_bf16(aK[1], ak, b[2], b[3]);
+        mma_bf16(aQ[0], aq, b[0], b[1]);
+        mma_bf16(aQ[1], aq, b[2], b[3]);
         if (need1) {
           load_b_nk(b, s.K, LDK, 32 * ch + 16, kk, lane);
-          mma_f16(aK[2], ak, b[0], b[1]);
-          mma_f16(aK[3], ak, b[2], b[3]);
-          mma_f16(aQ[2], aq, b[0], b[1]);
-          mma_f16(aQ[3], aq, b[2], b[3]);
+          mma_bf16(aK[2], ak, b[0], b[1]);
+          mma_bf16(aK[3], ak, b[2], b[3]);
+          mma_bf16(aQ[2], aq, b[0], b[1]);
+          mma_bf16(aQ[3], aq, b[2], b[3]);
         }
       }
     }
@@ -181,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
     for (int i = tid; i < kC * (DK / 8); i += kThreads) {
       const int r = i / (DK / 8), sg = i % (DK / 8);
       *reinterpret_cast<uint4*>(Qt + swz<DK>(r, sg * 8)) =
-          scale_f16x8(&s.Q[r * LDK + sg * 8], p.scale * s.gam[r]);
-      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, sg * 8)) = scale_f16x8(&s.K[r * LDK + sg * 8], s.e[r]);
+          scale_bf16x8_to_f16(&s.Q[r * LDK + sg * 8], p.scale * s.gam[r]);
+      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, sg * 8)) =
+          scale_bf16x8_to_f16(&s.K[r * LDK + sg * 8], s.e[r]);
     }
     __syncthreads();  // Q is dead: its storage becomes A
     GDN_PHASE(3);  // Qt, Kt
@@ -203,22 +205,39 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
           s.A[r * LDA + cc] = av[y];
         }
         *reinterpret_cast<uint32_t*>(&s.Ah[r * LDC + c0]) = pack_f16(av[0], av[1]);
-        *reinterpret_cast<uint32_t*>(Pout + swz<kC>(r, c0)) = pack_f16(pv[0], pv[1]);
+        *reinterpret_cast<uint32_t*>(&s.Pst[swz<kC>(r, c0)]) = pack_f16(pv[0], pv[1]);
       }
     }
+    fence_proxy_async();  // P staging is read by a bulk store
   }
   __syncthreads();
 
   GDN_PHASE(4);  // masks
-  // ---- #3 Solve and the scaled fp16 operands --------------------------------
+  // ---- #3 Solve and the scaled operands --------------------------------------
+  if (tid == 0) {  // P leaves in one bulk store while the solve runs
+    fence_proxy_async();
+    bulk_s2g(Pout, s.Pst, kC * kC * 2);
+    bulk_commit();
+  }
   solve_unit_lower_64(s.A, LDA, s.Ah, s.Tm, LDA, s.Th, LDC);
+  if (tid == 0) bulk_wait_read<0>();
+  __syncthreads();  // P staging is free: Tw takes its place
   GDN_PHASE(5);  // solve
-  for (int e = tid; e < kC * kC; e += kThreads) {
-    const int r = e >> 6, cc = e & 63;
-    const float tv = s.Tm[r * LDA + cc];
-    const float b = s.beta[cc];
-    s.Tw[r * LDC + cc] = __float2half_rn(tv * b * s.gam[cc]);
-    s.Tu[r * LDC + cc] = __float2half_rn(tv * b);
+  for (int e = tid; e < kC * (kC / 8); e += kThreads) {  // 8 columns per item, 16-byte stores
+    const int r = e >> 3, c0 = (e & 7) * 8;
+    uint4 w, u;
+    __nv_bfloat162* wp = reinterpret_cast<__nv_bfloat162*>(&w);
+    __half2* up = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int cc = c0 + 2 * x;
+      const float t0 = s.Tm[r * LDA + cc], t1 = s.Tm[r * LDA + cc + 1];
+      const float b0 = s.beta[cc], b1 = s.beta[cc + 1];
+      wp[x] = __floats2bfloat162_rn(t0 * b0 * s.gam[cc], t1 * b1 * s.gam[cc + 1]);
+      up[x] = __floats2half2_rn(t0 * b0, t1 * b1);
+    }
+    *reinterpret_cast<uint4*>(&s.Tw[r * LDC + c0]) = w;
+    *reinterpret_cast<uint4*>(&s.Tu[r * LDC + c0]) = u;
   }
   __syncthreads();
   GDN_PHASE(6);  // Tw, Tu
@@ -242,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
 #pragma unroll
       for (int j = 0; j < WNT; j += 2) {
         load_b_kn(b, s.K, LDK, nh * (DK / 2) + 8 * j, kk, lane);
-        mma_f16(aW[j], a, b[0], b[1]);
-        mma_f16(aW[j + 1], a, b[2], b[3]);
+        mma_bf16(aW[j], a, b[0], b[1]);
+        mma_bf16(aW[j + 1], a, b[2], b[3]);
       }
       load_a(a, s.Tu, LDC, 16 * rb, kk, lane);
 #pragma unroll
