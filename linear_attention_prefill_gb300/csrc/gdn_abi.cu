@@ -131,12 +131,17 @@ gdn_status run_fwd_f32(const gdn::FwdParams& p, cudaStream_t stream) {
   return GDN_OK;
 }
 
-gdn_status launch_three(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream);
+gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream);
 
-// bf16 forward: chunk-parallel prep launch, chunk-serial chain launch, chunk-parallel output launch.
+// bf16 forward: the chunk-parallel prep launch, then the chunk-serial chain launch
+// (which also writes the output).
 gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaStream_t stream) {
   if (p.N == 0) return GDN_OK;
   if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
+  // tensor-map row coordinates are 32-bit
+  if ((p.cu_seqlens ? 1ll : (long long)p.N) * p.T > 0x7fffffffll)
+    return fail(GDN_ERR_UNSUPPORTED, "%lld tokens: the bf16 path takes at most 2^31 - 1",
+                (p.cu_seqlens ? 1ll : (long long)p.N) * p.T);
   const gdn::WsLayout w = gdn::ws_layout(p, ws);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % 256) != 0 || ws_size < gdn::ws_bytes(w, p.Hv))
     return fail(GDN_ERR_INVALID_ARG, "workspace %p of %zu bytes: need %zu bytes, 256-byte aligned",
@@ -144,16 +149,14 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
   gdn::FwdParams q = p;
   cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&q.err), gdn::g_device_error);
   if (e != cudaSuccess) return cuda_fail(e, "locating the device error word");
-  return launch_three(q, w, stream);
+  return launch_pipeline(q, w, stream);
 }
 
-gdn_status launch_three(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
+gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
   cudaError_t e = gdn::launch_prep(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
   e = gdn::launch_chain(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the chain kernel");
-  e = gdn::launch_out(p, w, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "launching the output kernel");
   return GDN_OK;
 }
 

@@ -1,58 +1,93 @@
-// gdn_chain.cu - the serial Reduce (#5 H) of the chunkwise forward
-// ("Empowering Hybrid Attention Models on NPUs", §2.1, Figure 1(b)), split as in
-// §5 (Figure 10(b)) into the state read and the in-place update:
+// gdn_chain.cu - the serial Reduce (#5 H) and the final Map (#6 O) of the
+// chunkwise forward ("Empowering Hybrid Attention Models on NPUs", §2.1,
+// Figure 1(b)), the state update split as in §5 (Figure 10(b)) into the state
+// read and the in-place update:
 //   #5 read    V_new = U - W h
 //   #5 update  h = gamma_last h + Kt^T V_new        (Kt = diag(e) K)
+//   #6 O       O = diag(scale gamma) Q h + P V_new  (h: the state entering the chunk)
 // One CTA per (sequence, v head, dv tile) walks the chunks of its sequence in
 // order with its fp32 state tile h[:, tile] in registers: the column split of
 // the state (§4, Figure 8(b)) gives parallelism without any reduction.
 //
 // Warp roles.  Warps 0-3 run the chain: two warp-level fp16 tensor-core
 // products per chunk (mma.sync, the state as accumulator) and two CTA-local
-// barriers - nothing else sits on the serial path.  Warp 4 is the producer: it
-// stages W, Kt, the U tile and gamma_last of chunk c + 3 with bulk copies into a
-// 3-deep ring (36 KB per chunk at d = 128: one SM takes in about 64 bytes per
-// clock from L2, which bounds the step), and publishes the state entering each
-// chunk (H) and V_new with bulk stores for gdn_out.  The roles meet only at
-// mbarriers; every wait is bounded and an expired wait ends the CTA cleanly.
+// barriers - nothing else sits on the serial path.  They leave the state
+// entering each chunk (fp16) and V_new in a 3-deep shared-memory ring, from
+// which warps 4-7 compute that chunk's output tile one or two chunks behind,
+// so neither ever travels through HBM.  Warp 8 is the producer: it stages W^T,
+// Kt, P, the U^T tile and the gate factors of chunk c + 3 with bulk copies and
+// the chunk's q rows with a TMA tensor load into a 3-deep ring.  The roles meet
+// only at mbarriers; every wait is bounded and an expired wait ends the CTA
+// cleanly.
+//
+// Precision: every product takes fp16 operands with fp32 accumulation; the
+// output warps scale their bf16 q fragments by scale gamma_i and round them to
+// fp16 in registers, so q needs no converted copy anywhere.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kC = 64;
-constexpr int kComputeThreads = 128;  // warps 0-3
-constexpr int kThreads = 160;         // + producer warp
+constexpr int kComputeThreads = 128;  // warps 0-3: the chain
+constexpr int kOutWarp0 = 4;          // warps 4-7: the output
+constexpr int kProducerWarp = 8;
+constexpr int kThreads = 288;
 constexpr int kStages = 3;
-constexpr int kPub = 3;  // H / V_new buffers: the store of chunk c - 1 has a whole step to finish
+constexpr int kPub = 3;  // state / V_new buffers shared with the output warps
 
+// Shared-memory map (byte offsets from a 1024-aligned base).
 template <int DK, int DVT>
-struct ChainSmem {
-  struct Stage {
-    __half W[kC * DK];    // swz<DK>
-    __half Kt[kC * DK];   // swz<DK>
-    __half U[kC * DVT];   // plain
-    float gl[4];
-  };
-  Stage st[kStages];
-  __half H[kPub][DK * DVT];   // swz<DVT>: state entering the chunk (ring for the stores)
-  __half Vn[kPub][kC * DVT];  // swz<DVT>
-  uint64_t full[kStages];     // producer -> chain: chunk staged (transaction bytes)
-  uint64_t empty[kStages];    // chain -> producer: stage consumed (4 warp arrivals)
-  uint64_t pub[kPub];         // chain -> producer: H[b], Vn[b] ready to store
-  uint64_t pubd[kPub];        // producer -> chain: H[b], Vn[b] read by the store
-  int abort;
+struct ChainLayout {
+  // one stage: q rows (bf16, 128-byte swizzle, [DK/64][64][64]) first for the
+  // 1024-byte alignment the swizzle needs, then the workspace record pieces
+  static constexpr int kQ = 0;
+  static constexpr int kWt = kQ + kC * DK * 2;   // W^T [DK][64] swz<64>
+  static constexpr int kKt = kWt + kC * DK * 2;  // Kt [64][DK] swz<DK>
+  static constexpr int kP = kKt + kC * DK * 2;   // P [64][64] swz<64>
+  static constexpr int kUt = kP + kC * kC * 2;   // U^T [DVT][64]
+  static constexpr int kGv = kUt + DVT * kC * 2; // gamma_last, pad, gamma[64]
+  static constexpr int kStageBytes = (kGv + kGvFloats * 4 + 1023) / 1024 * 1024;
+  static constexpr int kH = kStages * kStageBytes;      // [kPub][DK][DVT] fp16 swz<DVT>
+  static constexpr int kVn = kH + kPub * DK * DVT * 2;  // [kPub][64][DVT] fp16 swz<DVT>
+  static constexpr int kBar = kVn + kPub * kC * DVT * 2;
+  static constexpr int kBytes = kBar + 8 * (2 * kStages + 2 * kPub) + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base
+  static constexpr unsigned kTx = 3 * kC * DK * 2 + kC * kC * 2 + DVT * kC * 2 + kGvFloats * 4;
 };
 
+// A fragment (16x16) of a bf16 tile in the 128-byte-swizzled [k/64][rows][64] layout.
+__device__ __forceinline__ void load_a_sw128(uint32_t (&a)[4], const unsigned char* base, int m0,
+                                             int k0, int lane) {
+  const int r = m0 + (lane & 15), k = k0 + ((lane >> 4) << 3);
+  ldsm_x4(a[0], a[1], a[2], a[3],
+          base + (k >> 6) * 8192 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+// bf16 pair times s, rounded once to an fp16 pair
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t x, float s) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
+  return pack_f16(f.x * s, f.y * s);
+}
+
 template <int DK, int DVT>
-__global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams p, WsLayout ws) {
-  using S = ChainSmem<DK, DVT>;
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_chain_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq) {
+  using Lo = ChainLayout<DK, DVT>;
   constexpr int NT = DVT / 8;          // n8 tiles over the dv tile
-  constexpr int MTW = DK / 64;         // m16 tiles of the state per warp
-  constexpr unsigned kStageBytes = 2 * kC * DK * 2 + kC * DVT * 2 + 16;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  S& s = *reinterpret_cast<S*>(smem_raw);
+  constexpr int MTW = DK / 64;         // m16 tiles of the state per chain warp
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __half* Hring = reinterpret_cast<__half*>(sm + Lo::kH);
+  __half* Vring = reinterpret_cast<__half*>(sm + Lo::kVn);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lo::kBar);  // producer -> consumers
+  uint64_t* empty = full + kStages;  // 4 chain + 4 output warp arrivals: stage consumed
+  uint64_t* pub = empty + kStages;   // chain -> output: H[b], Vn[b] ready
+  uint64_t* pubd = pub + kPub;       // output -> chain: H[b], Vn[b] consumed (4 arrivals)
+  volatile int* s_abort = reinterpret_cast<volatile int*>(pubd + kPub);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
@@ -61,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
   const int dvt = blockIdx.x % n_dvt;
   const int hv = (blockIdx.x / n_dvt) % p.Hv;
   const int n = blockIdx.x / (n_dvt * p.Hv);
+  const int hq = hv / (p.Hv / p.Hqk);
   const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
   const long long len = p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
   const int n_chunks = (int)((len + kC - 1) / kC);
@@ -68,14 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 4);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 8);
     }
     for (int i = 0; i < kPub; ++i) {
-      mbar_init(&s.pub[i], 1);
-      mbar_init(&s.pubd[i], 1);
+      mbar_init(&pub[i], 1);
+      mbar_init(&pubd[i], 4);
     }
-    s.abort = 0;
+    *s_abort = 0;
     mbar_fence_init();
   }
 
@@ -95,42 +131,109 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
           b = *reinterpret_cast<const float2*>(h0 + (long long)(r0 + 8) * p.dv + col);
         }
         hacc[mt][j][0] = a.x; hacc[mt][j][1] = a.y; hacc[mt][j][2] = b.x; hacc[mt][j][3] = b.y;
-        *reinterpret_cast<uint32_t*>(&s.H[0][swz<DVT>(r0, col)]) = pack_f16(a.x, a.y);
-        *reinterpret_cast<uint32_t*>(&s.H[0][swz<DVT>(r0 + 8, col)]) = pack_f16(b.x, b.y);
+        *reinterpret_cast<uint32_t*>(&Hring[swz<DVT>(r0, col)]) = pack_f16(a.x, a.y);
+        *reinterpret_cast<uint32_t*>(&Hring[swz<DVT>(r0 + 8, col)]) = pack_f16(b.x, b.y);
       }
   }
   __syncthreads();  // barriers initialised, H[0] written
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ======================= producer ======================================
     if (lane == 0) {
       auto issue = [&](int c) {
-        typename S::Stage& b = s.st[c % kStages];
-        uint64_t* bar = &s.full[c % kStages];
-        mbar_expect_tx(bar, kStageBytes);
-        bulk_g2s(b.W, ws.W(slot0 + c, hv, p.Hv), kC * DK * 2, bar);
-        bulk_g2s(b.Kt, ws.Kt(slot0 + c, hv, p.Hv), kC * DK * 2, bar);
-        bulk_g2s(b.U, ws.U(slot0 + c, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
-        bulk_g2s(b.gl, ws.gl(slot0 + c, hv, p.Hv), 16, bar);
+        unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
+        uint64_t* bar = &full[c % kStages];
+        const long long slot = slot0 + c;
+        mbar_expect_tx(bar, Lo::kTx);
+        bulk_g2s(st + Lo::kWt, ws.W(slot, hv, p.Hv), kC * DK * 2, bar);
+        bulk_g2s(st + Lo::kKt, ws.Kt(slot, hv, p.Hv), kC * DK * 2, bar);
+        bulk_g2s(st + Lo::kP, ws.P(slot, hv, p.Hv), kC * kC * 2, bar);
+        bulk_g2s(st + Lo::kUt, ws.U(slot, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
+        bulk_g2s(st + Lo::kGv, ws.gv(slot, hv, p.Hv), kGvFloats * 4, bar);
+        const int row = (int)(t_seq + (long long)c * kC);
+#pragma unroll
+        for (int kb = 0; kb < DK / 64; ++kb)
+          tma_load_2d(st + Lo::kQ + kb * 8192, &tmq, hq * DK + kb * 64, row, bar);
       };
       for (int c = 0; c < kStages && c < n_chunks; ++c) issue(c);
-      for (int c = 0; c < n_chunks; ++c) {
-        const int hb = c % kPub;
-        // publish the state entering chunk c and its V_new
-        if (!mbar_wait(&s.pub[hb], (c / kPub) & 1, p.err)) { s.abort = 1; break; }
-        bulk_s2g(ws.H(slot0 + c, hv, p.Hv) + dvt * DK * DVT, s.H[hb], DK * DVT * 2);
-        bulk_s2g(ws.Vn(slot0 + c, hv, p.Hv) + dvt * kC * DVT, s.Vn[hb], kC * DVT * 2);
-        bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(&s.pubd[hb]);
-        // refill the stage chunk c used with chunk c + 3
-        if (c + kStages < n_chunks) {
-          if (!mbar_wait(&s.empty[c % kStages], (c / kStages) & 1, p.err)) { s.abort = 1; break; }
-          issue(c + kStages);
-        }
-        if (s.abort) break;
+      for (int c = 0; c + kStages < n_chunks; ++c) {
+        // refill the stage chunk c used with chunk c + 3 once both roles are done with it
+        if (!mbar_wait(&empty[c % kStages], (c / kStages) & 1, p.err)) { *s_abort = 1; break; }
+        if (*s_abort) break;
+        issue(c + kStages);
       }
-      bulk_wait<0>();
+    }
+    return;
+  }
+
+  if (warp >= kOutWarp0) {
+    // ======================= output (warps 4-7) =============================
+    // O[16 ow .. 16 ow + 15][tile] = diag(scale gamma) Q h + P V_new
+    const int ow = warp - kOutWarp0, m0 = 16 * ow;
+    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.o) + (long long)hv * p.dv + dvt * DVT;
+    const long long o_tok = (long long)p.Hv * p.dv;
+    for (int c = 0; c < n_chunks; ++c) {
+      const unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
+      const int hb = c % kPub;
+      if (!mbar_wait(&full[c % kStages], (c / kStages) & 1, p.err)) *s_abort = 1;
+      if (!*s_abort && !mbar_wait(&pub[hb], (c / kPub) & 1, p.err)) *s_abort = 1;
+      if (*s_abort) break;
+      const __half* H = Hring + hb * DK * DVT;
+      const __half* Vn = Vring + hb * kC * DVT;
+      float acc[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[j][x] = 0.f;
+      // inter-chunk term (diag(scale gamma) Q) h: the bf16 q fragments of rows
+      // gq and gq + 8 are scaled and rounded to fp16 in registers
+      const float* gv = reinterpret_cast<const float*>(st + Lo::kGv);
+      const float s0 = p.scale * gv[4 + m0 + gq], s1 = p.scale * gv[4 + m0 + gq + 8];
+#pragma unroll
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        uint32_t a[4];
+        load_a_sw128(a, st + Lo::kQ, m0, 16 * ks, lane);
+        a[0] = bf16x2_to_f16x2_scaled(a[0], s0);
+        a[1] = bf16x2_to_f16x2_scaled(a[1], s1);
+        a[2] = bf16x2_to_f16x2_scaled(a[2], s0);
+        a[3] = bf16x2_to_f16x2_scaled(a[3], s1);
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+          uint32_t bb[4];
+          load_b_kn_sw<DVT>(bb, H, 8 * j, 16 * ks, lane);
+          mma_f16(acc[j], a, bb[0], bb[1]);
+          mma_f16(acc[j + 1], a, bb[2], bb[3]);
+        }
+      }
+      // intra-chunk term P V_new (P lower triangular: k <= this row block)
+      const __half* P = reinterpret_cast<const __half*>(st + Lo::kP);
+      for (int kk = 0; kk <= m0; kk += 16) {
+        uint32_t a[4];
+        load_a_sw<kC>(a, P, m0, kk, lane);
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+          uint32_t bb[4];
+          load_b_kn_sw<DVT>(bb, Vn, 8 * j, kk, lane);
+          mma_f16(acc[j], a, bb[0], bb[1]);
+          mma_f16(acc[j + 1], a, bb[2], bb[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {  // this warp is done with H[hb], Vn[hb] and the stage
+        mbar_arrive(&pubd[hb]);
+        mbar_arrive(&empty[c % kStages]);
+      }
+      const long long t0 = t_seq + (long long)c * kC;
+      const int L = (int)min((long long)kC, len - (long long)c * kC);
+      const int r0 = m0 + gq, r1 = r0 + 8;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int col = 8 * j + 2 * tq;
+        if (r0 < L)
+          *reinterpret_cast<uint32_t*>(og + (t0 + r0) * o_tok + col) = pack_bf16(acc[j][0], acc[j][1]);
+        if (r1 < L)
+          *reinterpret_cast<uint32_t*>(og + (t0 + r1) * o_tok + col) = pack_bf16(acc[j][2], acc[j][3]);
+      }
     }
     return;
   }
@@ -141,20 +244,26 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
   // The A fragments of W and Kt are read before the state they multiply is ready.
   int c = 0;
   for (; c < n_chunks; ++c) {
-    typename S::Stage& b = s.st[c % kStages];
+    const unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
+    const __half* Wt = reinterpret_cast<const __half*>(st + Lo::kWt);
+    const __half* Kt = reinterpret_cast<const __half*>(st + Lo::kKt);
+    const __half* Ut = reinterpret_cast<const __half*>(st + Lo::kUt);
     const int hb = c % kPub, hn = (c + 1) % kPub;
+    __half* Hc = Hring + hb * DK * DVT;
+    __half* Hn = Hring + hn * DK * DVT;
+    __half* Vc = Vring + hb * kC * DVT;
     GDN_PHASE(16);  // loop top
-    if (!mbar_wait(&s.full[c % kStages], (c / kStages) & 1, p.err)) s.abort = 1;
+    if (!mbar_wait(&full[c % kStages], (c / kStages) & 1, p.err)) *s_abort = 1;
     GDN_PHASE(17);  // wait for staging
     uint32_t wa[DK / 16][4];  // W rows of this warp, all k steps
 #pragma unroll
-    for (int ks = 0; ks < DK / 16; ++ks) load_a_sw<DK>(wa[ks], b.W, 16 * warp, 16 * ks, lane);
+    for (int ks = 0; ks < DK / 16; ++ks) load_a_trans_sw<kC>(wa[ks], Wt, 16 * warp, 16 * ks, lane);
     uint32_t ka[kC / 16][MTW][4];  // Kt^T rows of this warp, all k steps
 #pragma unroll
     for (int ks = 0; ks < kC / 16; ++ks)
 #pragma unroll
       for (int mt = 0; mt < MTW; ++mt)
-        load_a_trans_sw<DK>(ka[ks][mt], b.Kt, 16 * (MTW * warp + mt), 16 * ks, lane);
+        load_a_trans_sw<DK>(ka[ks][mt], Kt, 16 * (MTW * warp + mt), 16 * ks, lane);
 
     // #5 read: V_new = U - W h   (warp: 16 token rows x the dv tile)
     const int r0 = 16 * warp + gq;
@@ -174,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
           for (int j = 0; j < NT; j += 2) {
             uint32_t bb[4];
-            load_b_kn_sw<DVT>(bb, s.H[hb], 8 * j, kk, lane);
+            load_b_kn_sw<DVT>(bb, Hc, 8 * j, kk, lane);
             mma_f16(wh[hh][j], wa[kk / 16], bb[0], bb[1]);
             mma_f16(wh[hh][j + 1], wa[kk / 16], bb[2], bb[3]);
           }
@@ -183,24 +292,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int col = 8 * j + 2 * tq;
-        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&b.U[r0 * DVT + col]));
-        const float2 u1 =
-            __half22float2(*reinterpret_cast<const __half2*>(&b.U[(r0 + 8) * DVT + col]));
-        *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0, col)]) =
+        const float2 u0 = make_float2(__half2float(Ut[col * kC + r0]),
+                                      __half2float(Ut[(col + 1) * kC + r0]));
+        const float2 u1 = make_float2(__half2float(Ut[col * kC + r0 + 8]),
+                                      __half2float(Ut[(col + 1) * kC + r0 + 8]));
+        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0, col)]) =
             pack_f16(u0.x - wh[0][j][0] - wh[1][j][0], u0.y - wh[0][j][1] - wh[1][j][1]);
-        *reinterpret_cast<uint32_t*>(&s.Vn[hb][swz<DVT>(r0 + 8, col)]) =
+        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0 + 8, col)]) =
             pack_f16(u1.x - wh[0][j][2] - wh[1][j][2], u1.y - wh[0][j][3] - wh[1][j][3]);
       }
     }
-    fence_proxy_async();
     named_sync(1, kComputeThreads);  // V_new complete (H[hb] was complete before)
     GDN_PHASE(20);  // V_new
-    if (s.abort) break;
-    if (tid == 0) mbar_arrive(&s.pub[hb]);
+    if (*s_abort) break;
+    if (tid == 0) mbar_arrive(&pub[hb]);
 
     // #5 update: h = gamma_last h + Kt^T V_new, written straight into H[hn]
     {
-      const float gl = b.gl[0];
+      const float gl = reinterpret_cast<const float*>(st + Lo::kGv)[0];
 #pragma unroll
       for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
@@ -212,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
           uint32_t bb[4];
-          load_b_kn_sw<DVT>(bb, s.Vn[hb], 8 * j, 16 * ks, lane);
+          load_b_kn_sw<DVT>(bb, Vc, 8 * j, 16 * ks, lane);
 #pragma unroll
           for (int mt = 0; mt < MTW; ++mt) {
             mma_f16(hacc[mt][j], ka[ks][mt], bb[0], bb[1]);
@@ -222,28 +331,28 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s.empty[c % kStages]);  // this warp is done with the stage
+    if (lane == 0) mbar_arrive(&empty[c % kStages]);  // this warp is done with the stage
     GDN_PHASE(22);  // update
-    // H[hn] last held the state entering chunk c - 2: its store must have read it
-    if (c >= 2 && !mbar_wait(&s.pubd[hn], ((c - 2) / kPub) & 1, p.err)) s.abort = 1;
+    // H[hn] last held the state entering chunk c - 2: the output warps must be done with it
+    if (c >= 2 && !mbar_wait(&pubd[hn], ((c - 2) / kPub) & 1, p.err)) *s_abort = 1;
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int hr = 16 * (MTW * warp + mt) + gq, col = 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&s.H[hn][swz<DVT>(hr, col)]) =
+        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr, col)]) =
             pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
-        *reinterpret_cast<uint32_t*>(&s.H[hn][swz<DVT>(hr + 8, col)]) =
+        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr + 8, col)]) =
             pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
       }
     named_sync(1, kComputeThreads);  // next state copy complete
     GDN_PHASE(23);  // state copy
   }
-  if (tid == 0 && s.abort) {  // a wait gave up: let the copies already issued land
+  if (tid == 0 && *s_abort) {  // a wait gave up: let the copies already issued land
     for (int cc = c + 1; cc < min(c + kStages, n_chunks); ++cc)
-      mbar_wait(&s.full[cc % kStages], (cc / kStages) & 1, nullptr);
+      mbar_wait(&full[cc % kStages], (cc / kStages) & 1, nullptr);
   }
-  if (p.hT && !s.abort) {
+  if (p.hT && !*s_abort) {
     float* hT = p.hT + ((long long)(n * p.Hv + hv) * DK) * p.dv + dvt * DVT;
 #pragma unroll
     for (int mt = 0; mt < MTW; ++mt)
@@ -260,20 +369,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chain_kernel(const FwdParams 
 
 template <int DK, int DVT>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
-  const size_t smem = sizeof(ChainSmem<DK, DVT>);
+  using Lo = ChainLayout<DK, DVT>;
+  const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
+  CUtensorMap mq;
+  if (!make_tensor_map_bf16(&mq, p.q, rows, (long long)p.Hqk * DK)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
-  gdn_chain_kernel<DK, DVT><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
+  gdn_chain_kernel<DK, DVT><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
   return cudaGetLastError();
 }
 
 template <int DK>
 cudaError_t launch_dk(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
   if (ws.dvt == 16) return launch_t<DK, 16>(p, ws, stream);
-  if (ws.dvt == 32) return launch_t<DK, 32>(p, ws, stream);
-  return launch_t<DK, 64>(p, ws, stream);
+  return launch_t<DK, 32>(p, ws, stream);
 }
 
 }  // namespace

@@ -17,7 +17,16 @@
 // the library build, where the marks compile to nothing.
 #ifdef GDN_PROFILE
 extern __device__ unsigned long long g_gdn_phase[64];  // defined in gdn_abi.cu; needs -rdc
-#define GDN_PHASE_INIT long long gdn_phase_t = clock64()
+#define GDN_PHASE_INIT \
+  long long gdn_phase_t = clock64(); \
+  const long long gdn_phase_start = gdn_phase_t; \
+  (void)gdn_phase_start
+// cycles since the CTA started, added to g_gdn_phase[id] by thread t only
+#define GDN_STAMP(id, t)                                                            \
+  do {                                                                             \
+    if (threadIdx.x == (t))                                                        \
+      atomicAdd(&g_gdn_phase[(id)], (unsigned long long)(clock64() - gdn_phase_start)); \
+  } while (0)
 #define GDN_PHASE(id)                                                              \
   do {                                                                             \
     if (threadIdx.x == 0) {                                                        \
@@ -28,6 +37,9 @@ extern __device__ unsigned long long g_gdn_phase[64];  // defined in gdn_abi.cu;
   } while (0)
 #else
 #define GDN_PHASE_INIT
+#define GDN_STAMP(id, t) \
+  do {                   \
+  } while (0)
 #define GDN_PHASE(id) \
   do {                \
   } while (0)

@@ -1,6 +1,7 @@
 // gdn_internal.h - launch parameters shared by the C ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,32 +39,32 @@ struct StepParams {
   float scale;
 };
 
-// Workspace of the bf16 forward: one record per (chunk slot, v head), all fp16
-// row-major with 16-byte chunks XOR-swizzled per row (gdn::swz<width>), so a
-// verbatim bulk copy lands in shared memory ready for conflict-free ldmatrix:
-//   W    [64][dk]         Tm diag(beta gamma) K                  (gdn_prep)
-//   Kt   [64][dk]         diag(e) K, e_j = exp(G_last - G_j)     (gdn_prep)
-//   Qt   [64][dk]         diag(scale gamma) Q                    (gdn_prep)
-//   P    [64][64]         tril(scale exp(G_i - G_j) q_i.k_j)     (gdn_prep)
-//   U    [dv/t][64][t]    Tm diag(beta) V, one block per t-column dv tile, not swizzled
-//   gl   fp32 + pad       gamma_last = exp(G_last)               (gdn_prep)
-//   H    [dv/t][dk][t]    state entering the chunk, per dv tile  (gdn_chain)
-//   Vn   [dv/t][64][t]    V_new = U - W h, per dv tile           (gdn_chain)
-// The dv tile t (16, 32 or 64 columns, one chain CTA each) is picked per call
-// by dv_tile(): the narrowest that still leaves at most ~one CTA per SM, since
-// every chain CTA must take in the whole W and Kt of its chain.
-// gdn_out reads Qt, P, H and Vn.  Sequence n's chunk c lives in slot
-// first_slot(n) + c: n * ceil(T / 64) for fixed-length rows; floor(cu[n] / 64) +
-// n with cu_seqlens, which never overlaps because floor((a + L) / 64) -
-// floor(a / 64) + 1 >= ceil(L / 64), and ends below floor(T / 64) + N + 1.
+// Workspace of the bf16 forward: one record per (chunk slot, v head), written
+// by gdn_prep and read by gdn_chain.  16-bit tiles are row-major with their
+// 16-byte chunks XOR-swizzled per row (gdn::swz<width>), so a verbatim bulk
+// copy lands in shared memory ready for conflict-free ldmatrix:
+//   W    [dk][64]   W^T, W = Tm diag(beta gamma) K, swz<64>, fp16
+//   Kt   [64][dk]   diag(e) K, e_j = exp(G_last - G_j), swz<dk>, fp16
+//   P    [64][64]   tril(scale exp(G_i - G_j) q_i.k_j), swz<64>, fp16
+//   U    [dv][64]   U^T, U = Tm diag(beta) V, fp16, not swizzled: the t-column
+//                   dv tile j is the contiguous rows [j t, (j + 1) t)
+//   gv   fp32 [68]  gamma_last, 3 pad, gamma_i = exp(G_i) for the 64 rows
+// The dv tile t (16 or 32 columns, one chain CTA each) is picked per call by
+// dv_tile(): the narrowest that still leaves at most ~one CTA per SM, since
+// every chain CTA must take in the whole W, Kt, P and q of each chunk.
+// Sequence n's chunk c lives in slot first_slot(n) + c: n * ceil(T / 64) for
+// fixed-length rows; floor(cu[n] / 64) + n with cu_seqlens, which never
+// overlaps because floor((a + L) / 64) - floor(a / 64) + 1 >= ceil(L / 64), and
+// ends below floor(T / 64) + N + 1.
 constexpr int kChunk = 64;
+constexpr int kGvFloats = 68;
 
 struct WsLayout {
   char* base;
   int dvt;                  // dv tile width of the chain launch
   long long n_slots;        // chunk slots per v head
   long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
-  long long task_bytes, kt_off, qt_off, p_off, u_off, gl_off, h_off, vn_off;
+  long long task_bytes, kt_off, p_off, u_off, gv_off;
 
   __host__ __device__ char* rec(long long slot, int hv, int Hv) const {
     return base + (slot * Hv + hv) * task_bytes;
@@ -74,23 +75,14 @@ struct WsLayout {
   __host__ __device__ __half* Kt(long long s, int hv, int Hv) const {
     return reinterpret_cast<__half*>(rec(s, hv, Hv) + kt_off);
   }
-  __host__ __device__ __half* Qt(long long s, int hv, int Hv) const {
-    return reinterpret_cast<__half*>(rec(s, hv, Hv) + qt_off);
-  }
   __host__ __device__ __half* P(long long s, int hv, int Hv) const {
     return reinterpret_cast<__half*>(rec(s, hv, Hv) + p_off);
   }
   __host__ __device__ __half* U(long long s, int hv, int Hv) const {
     return reinterpret_cast<__half*>(rec(s, hv, Hv) + u_off);
   }
-  __host__ __device__ float* gl(long long s, int hv, int Hv) const {
-    return reinterpret_cast<float*>(rec(s, hv, Hv) + gl_off);
-  }
-  __host__ __device__ __half* H(long long s, int hv, int Hv) const {
-    return reinterpret_cast<__half*>(rec(s, hv, Hv) + h_off);
-  }
-  __host__ __device__ __half* Vn(long long s, int hv, int Hv) const {
-    return reinterpret_cast<__half*>(rec(s, hv, Hv) + vn_off);
+  __host__ __device__ float* gv(long long s, int hv, int Hv) const {
+    return reinterpret_cast<float*>(rec(s, hv, Hv) + gv_off);
   }
   __device__ long long first_slot(const FwdParams& p, int n) const {
     if (p.cu_seqlens) return (long long)(p.cu_seqlens[n] / kChunk) + n;
@@ -99,12 +91,11 @@ struct WsLayout {
 };
 
 // dv tile of the chain launch: 16 columns while chains x dv/16 CTAs fit on the
-// 152 SMs, else 32, else 64 (and never wider than dv).
+// 152 SMs, else 32 (and never wider than dv).
 inline int dv_tile(const FwdParams& p) {
   const long long chains = (long long)p.N * p.Hv;
   if (chains * (p.dv / 16) <= 152) return 16;
-  if (chains * (p.dv / 32) <= 152 || p.dv == 32) return 32;
-  return 64;
+  return 32;
 }
 
 // Layout for one call (sizes validated); base may be null when only sizing.
@@ -121,13 +112,10 @@ inline WsLayout ws_layout(const FwdParams& p, void* base) {
   }
   const long long wk = (long long)kChunk * p.dk * 2, wv = (long long)kChunk * p.dv * 2;
   w.kt_off = wk;
-  w.qt_off = 2 * wk;
-  w.p_off = 3 * wk;
+  w.p_off = 2 * wk;
   w.u_off = w.p_off + (long long)kChunk * kChunk * 2;
-  w.gl_off = w.u_off + wv;
-  w.h_off = w.gl_off + 16;
-  w.vn_off = w.h_off + (long long)p.dk * p.dv * 2;
-  w.task_bytes = w.vn_off + wv;
+  w.gv_off = w.u_off + wv;
+  w.task_bytes = (w.gv_off + kGvFloats * 4 + 127) / 128 * 128;  // records on 128-byte lines
   return w;
 }
 inline size_t ws_bytes(const WsLayout& w, int Hv) { return (size_t)(w.n_slots * Hv * w.task_bytes); }
@@ -153,10 +141,13 @@ __device__ inline bool locate_chunk(const FwdParams& p, const WsLayout& ws, long
   return true;
 }
 
+// Tensor map of a row-major [rows, cols] bf16 matrix, boxes of 64 x 64 with the
+// 128-byte swizzle (gdn_prep.cu); false if the driver refuses it.
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols);
+
 // Launchers: return cudaSuccess or the launch error.  Each validates nothing.
 cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
-cudaError_t launch_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream);
 cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream);

@@ -6,56 +6,64 @@
 //   #1 Gate   G = cumsum(g), gamma = exp(G), e_j = exp(G_last - G_j)
 //   #2 KKT    A = tril_strict(beta_i exp(G_i - G_j) k_i.k_j)
 //      QK^T   P = tril(scale exp(G_i - G_j) q_i.k_j)
-//   #3 Solve  Tm = (I + A)^-1   (diagonal blocks by substitution, merges on tensor cores)
+//   #3 Solve  Tm = (I + A)^-1   (diagonal blocks by substitution, merges on mma.sync)
 //   #4 W/U    W = Tm diag(beta gamma) K,  U = Tm diag(beta) V
-// plus the two scaled copies the later launches consume: Kt = diag(e) K (the
-// state update's left factor) and Qt = diag(scale gamma) Q (the output's
-// inter-chunk term).  The serial Reduce (#5) runs in gdn_chain.cu, the final
-// Map (#6) in gdn_out.cu; both read this kernel's workspace records.
+// plus the scaled copy Kt = diag(e) K (the state update's left factor) and
+// the row factors gamma.  The serial Reduce (#5) and the final Map (#6) run in
+// gdn_chain.cu, which reads this kernel's workspace records.
 //
-// Tensor-core products accumulate in fp32.  The grams and W = (Tm diag(beta
-// gamma)) K take the bf16 inputs as they are (W's left factor rounded to bf16:
-// its share of the error is below 1e-3 of RMS); U = Tm diag(beta) V takes fp16
-// operands (v rewritten in place, exact in fp16's normal range), since U's
-// rounding feeds V_new and the output directly.
+// Blackwell mapping.  K and Q arrive by TMA in 128-byte-swizzled tiles stacked
+// as one 128-row operand [K; Q], so a single M = 128 tcgen05 MMA chain gives
+// both grams (K K^T in tensor-memory lanes 0-63, Q K^T in lanes 64-127).  The
+// same K tile, read MN-major, is the left factor of W^T = K^T (Tm diag(beta
+// gamma))^T, and V (loaded into the Q rows once Q is consumed) that of U^T:
+// the products come out transposed, one d index per tensor-memory lane, so each
+// thread writes whole 16-byte row segments of W^T and U^T.  Accumulators stay
+// in 128 tensor-memory columns and shared memory in ~72 KB, so three tasks
+// share an SM.  The triangular solve keeps its fp32 diagonal blocks and fp16
+// mma.sync merges, and writes the scaled MMA operands directly.
+//
+// Precision: products accumulate in fp32.  The grams and W take the bf16
+// inputs as they are (W's left factor rounded to bf16: its share of the error
+// is below 1e-3 of RMS); U takes fp16 operands (v rewritten in place, exact in
+// fp16's normal range), since U's rounding feeds V_new and the output directly.
+#include <cudaTypedefs.h>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kC = 64;
 constexpr int kThreads = 256;
+constexpr int kLDH = kC + 8;  // fp16 row stride of Ah and Th (conflict-free ldmatrix)
+constexpr float kLog2e = 1.4426950408889634f;
 
+// Shared-memory map (byte offsets from a 1024-aligned base).
 template <int DK, int DV>
-struct PrepSmem {
-  static constexpr int LDK = DK + 8;   // 16-bit row strides (conflict-free ldmatrix)
-  static constexpr int LDV = DV + 8;
-  static constexpr int LDC = kC + 8;
-  static constexpr int LDA = kC + 4;   // fp32 row stride of A and Tm
-  __half K[kC * LDK];                  // bf16 bits (grams and W take bf16 operands)
-  union {                              // Q (bf16 bits) until the grams are done, then A, then U staging
-    __half Q[kC * LDK];
-    float A[kC * LDA];
-    __half Ust[kC * LDV];
-  };
-  __half V[kC * LDV];
-  union {                              // Tm until Tw/Tu are built, then W staging
-    float Tm[kC * LDA];
-    __half Wst[kC * LDK];
-  };
-  __half Ah[kC * LDC];
-  __half Th[kC * LDC];
-  union {                              // P staging for its bulk store, then Tw (bf16 bits)
-    __half Pst[kC * kC];
-    __half Tw[kC * LDC];
-  };
-  __half Tu[kC * LDC];
-  float g[kC], beta[kC], G[kC], gam[kC], e[kC];
+struct PrepLayout {
+  // [DK/64][128 rows][64] bf16, 128-byte swizzle: rows 0-63 K, rows 64-127 Q
+  static constexpr int kKQBytes = (DK / 64) * 16384;
+  // V takes the Q rows once the grams are done (when it fits there)
+  static constexpr bool kVinQ = DV <= DK;
+  static constexpr int kV = kVinQ ? 8192 : kKQBytes;
+  static constexpr int kVStride = kVinQ ? 16384 : 8192;  // bytes between 64-column blocks
+  static constexpr int kTw = kKQBytes + (kVinQ ? 0 : (DV / 64) * 8192);  // bf16 [64][64] sw128
+  static constexpr int kTu = kTw + 8192;                                   // fp16 [64][64] sw128
+  static constexpr int kAh = kTu + 8192;                                   // fp16 [64][kLDH]
+  static constexpr int kTh = kAh + kC * kLDH * 2;                          // fp16 [64][kLDH]
+  static constexpr int kAd = kTh + kC * kLDH * 2;      // fp32 diagonal blocks of A [4][16][16]
+  static constexpr int kVec = kAd + 4 * 256 * 4;       // beta, G, gamma, e, beta*gamma [5][64]
+  static constexpr int kBar = kVec + 5 * kC * 4;       // 3 mbarriers, tmem address, abort flag
+  static constexpr int kBytes = kBar + 64;
+  static constexpr int kAlloc = kBytes + 1024;         // slack to align the base
+  static_assert(kTw % 1024 == 0 && kAh % 16 == 0 && kAd % 16 == 0, "alignment");
 };
 
 // 8 bf16 values at p (16-byte aligned) times `scale`, rounded once to fp16.
-__device__ __forceinline__ uint4 scale_bf16x8_to_f16(const __half* p, float scale) {
+__device__ __forceinline__ uint4 scale_bf16x8_to_f16(const void* p, float scale) {
   uint4 raw = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
   uint4 out;
@@ -68,12 +76,46 @@ __device__ __forceinline__ uint4 scale_bf16x8_to_f16(const __half* p, float scal
   return out;
 }
 
+__device__ __forceinline__ uint4 pack8_f16(const float* x) {
+  return make_uint4(pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]),
+                    pack_f16(x[6], x[7]));
+}
+
+// Store T(r, c) and T(r, c + 1) (c even) into the solve's outputs: the fp16
+// copy Th (when given) and the MMA operands Tw = T diag(beta gamma) (bf16) and
+// Tu = T diag(beta) (fp16).
+__device__ __forceinline__ void put_t2(__half* Th, __half* Tw, __half* Tu, const float* bg,
+                                       const float* beta, int r, int c, float t0, float t1) {
+  if (Th) *reinterpret_cast<uint32_t*>(&Th[r * kLDH + c]) = pack_f16(t0, t1);
+  *reinterpret_cast<uint32_t*>(&Tw[sw128(r, c)]) = pack_bf16(t0 * bg[c], t1 * bg[c + 1]);
+  *reinterpret_cast<uint32_t*>(&Tu[sw128(r, c)]) = pack_f16(t0 * beta[c], t1 * beta[c + 1]);
+}
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p, WsLayout ws) {
-  using S = PrepSmem<DK, DV>;
-  constexpr int LDK = S::LDK, LDV = S::LDV, LDC = S::LDC, LDA = S::LDA;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  S& s = *reinterpret_cast<S*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 3)
+    gdn_prep_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using Lo = PrepLayout<DK, DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(sm);
+  __half* Tw = reinterpret_cast<__half*>(sm + Lo::kTw);  // bf16 bits
+  __half* Tu = reinterpret_cast<__half*>(sm + Lo::kTu);
+  __half* Ah = reinterpret_cast<__half*>(sm + Lo::kAh);
+  __half* Th = reinterpret_cast<__half*>(sm + Lo::kTh);
+  float* Ad = reinterpret_cast<float*>(sm + Lo::kAd);
+  float* s_beta = reinterpret_cast<float*>(sm + Lo::kVec);
+  float* s_G = s_beta + kC;
+  float* s_gam = s_G + kC;
+  float* s_e = s_gam + kC;
+  float* s_bg = s_e + kC;
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + Lo::kBar);
+  uint64_t* bar_v = bar_kq + 1;
+  uint64_t* bar_mma = bar_kq + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kq + 3);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
@@ -82,51 +124,48 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
   const int hv = blockIdx.x % p.Hv;
   const long long slot = blockIdx.x / p.Hv;
   int n, c;
-  if (!locate_chunk(p, ws, slot, &n, &c)) return;
+  if (!locate_chunk(p, ws, slot, &n, &c)) return;  // before any allocation
   const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
   const long long len =
       p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
-  const long long t0 = t_seq + (long long)c * kC;
+  const int t0 = (int)(t_seq + (long long)c * kC);  // row in the flattened [tokens, H d] maps
   const int L = (int)min((long long)kC, len - (long long)c * kC);
   const int hq = hv / (p.Hv / p.Hqk);
 
-  // ---- staging (cp.async, zero-filled past the sequence end) ---------------
-  {
-    const long long qk_tok = (long long)p.Hqk * DK, v_tok = (long long)p.Hv * DV;
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k) + (long long)hq * DK;
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + (long long)hq * DK;
-    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v) + (long long)hv * DV;
-    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-      const int r = i / (DK / 8), sg = i % (DK / 8);
-      const bool ok = r < L;
-      const long long tok = t0 + (ok ? r : 0);
-      cp_async16(&s.K[r * LDK + sg * 8], kg + tok * qk_tok + sg * 8, ok);
-      cp_async16(&s.Q[r * LDK + sg * 8], qg + tok * qk_tok + sg * 8, ok);
+  // ---- setup: barriers, the K/Q (and a separate V) loads, tensor memory -----
+  if (tid == 0) {
+    mbar_init(bar_kq, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    *s_abort = 0;
+    mbar_fence_init();
+    mbar_expect_tx(bar_kq, 2u * kC * DK * 2);
+#pragma unroll
+    for (int kb = 0; kb < DK / 64; ++kb) {
+      tma_load_2d(sm + kb * 16384, &tmk, hq * DK + kb * 64, t0, bar_kq);
+      tma_load_2d(sm + kb * 16384 + 8192, &tmq, hq * DK + kb * 64, t0, bar_kq);
     }
-    for (int i = tid; i < kC * (DV / 8); i += kThreads) {
-      const int r = i / (DV / 8), sg = i % (DV / 8);
-      const bool ok = r < L;
-      const long long tok = t0 + (ok ? r : 0);
-      cp_async16(&s.V[r * LDV + sg * 8], vg + tok * v_tok + sg * 8, ok);
+    if (!Lo::kVinQ) {
+      mbar_expect_tx(bar_v, (unsigned)kC * DV * 2);
+#pragma unroll
+      for (int vb = 0; vb < DV / 64; ++vb)
+        tma_load_2d(sm + Lo::kV + vb * Lo::kVStride, &tmv, hv * DV + vb * 64, t0, bar_v);
+    } else {  // V's shared-memory slot frees up only after the grams: stage it in L2 now
+#pragma unroll
+      for (int vb = 0; vb < DV / 64; ++vb) tma_prefetch_2d(&tmv, hv * DV + vb * 64, t0);
     }
-    if (tid < kC) {
-      const bool ok = tid < L;
-      const long long tok = t0 + (ok ? tid : 0);
-      cp_async4(&s.g[tid], p.g + tok * p.Hv + hv, ok);
-      cp_async4(&s.beta[tid], p.beta + tok * p.Hv + hv, ok);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
   }
-  __syncthreads();
-  GDN_PHASE(0);  // staging
-  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // V -> fp16 (U takes fp16 operands)
-    const int r = i / (DV / 8), sg = i % (DV / 8);
-    bf16x8_to_f16x8(&s.V[r * LDV + sg * 8]);
-  }
-  // ---- #1 Gate (padded rows carry g = 0, so G[63] = G_last) ------------------
-  if (warp == 0) {
-    const float g0 = s.g[2 * lane], g1 = s.g[2 * lane + 1];
+  __syncwarp();
+  if (warp == 0) tmem_alloc(s_tmem, 128);
+  // ---- #1 Gate (rows past the sequence carry g = beta = 0, so G[63] = G_last)
+  if (warp == 1) {
+    const int r0 = 2 * lane, r1 = 2 * lane + 1;
+    const float* gp = p.g + (long long)t0 * p.Hv + hv;
+    const float* bp = p.beta + (long long)t0 * p.Hv + hv;
+    const float g0 = r0 < L ? gp[(long long)r0 * p.Hv] : 0.f;
+    const float g1 = r1 < L ? gp[(long long)r1 * p.Hv] : 0.f;
+    const float b0 = r0 < L ? bp[(long long)r0 * p.Hv] : 0.f;
+    const float b1 = r1 < L ? bp[(long long)r1 * p.Hv] : 0.f;
     float incl = g0 + g1;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -134,186 +173,342 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prep_kernel(const FwdParams p
       if (lane >= off) incl += y;
     }
     const float Glast = __shfl_sync(0xffffffffu, incl, 31);
-    s.G[2 * lane] = incl - g1;
-    s.G[2 * lane + 1] = incl;
-    s.gam[2 * lane] = expf(incl - g1);
-    s.gam[2 * lane + 1] = expf(incl);
-    s.e[2 * lane] = expf(Glast - (incl - g1));
-    s.e[2 * lane + 1] = expf(Glast - incl);
-    if (lane == 31) *ws.gl(slot, hv, p.Hv) = expf(Glast);
+    const float G0 = incl - g1, G1 = incl;
+    const float gam0 = expf(G0), gam1 = expf(G1);
+    s_G[r0] = G0;
+    s_G[r1] = G1;
+    s_gam[r0] = gam0;
+    s_gam[r1] = gam1;
+    s_e[r0] = expf(Glast - G0);
+    s_e[r1] = expf(Glast - G1);
+    s_beta[r0] = b0;
+    s_beta[r1] = b1;
+    s_bg[r0] = b0 * gam0;
+    s_bg[r1] = b1 * gam1;
+    float* gv = ws.gv(slot, hv, p.Hv);  // gamma_last, then gamma of every row
+    if (lane == 31) gv[0] = expf(Glast);
+    *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
   }
+  tc_fence_before();
   __syncthreads();
-  GDN_PHASE(1);  // convert + gate
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  GDN_PHASE(0);  // setup + gate
 
-  // ---- #2 KKT and QK^T grams (lower triangle) -------------------------------
-  __half* Pout = ws.P(slot, hv, p.Hv);
-  {
-    const int rb = warp >> 1, ch = warp & 1;
-    float aK[4][4], aQ[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) aK[j][x] = aQ[j][x] = 0.f;
-    const bool need0 = 2 * ch <= rb, need1 = 2 * ch + 1 <= rb;
-    if (need0) {
-#pragma unroll 2
-      for (int kk = 0; kk < DK; kk += 16) {
-        uint32_t ak[4], aq[4], b[4];
-        load_a(ak, s.K, LDK, 16 * rb, kk, lane);
-        load_a(aq, s.Q, LDK, 16 * rb, kk, lane);
-        load_b_nk(b, s.K, LDK, 32 * ch, kk, lane);
-        mma_bf16(aK[0], ak, b[0], b[1]);
-        mma_bf16(aK[1], ak, b[2], b[3]);
-        mma_bf16(aQ[0], aq, b[0], b[1]);
-        mma_bf16(aQ[1], aq, b[2], b[3]);
-        if (need1) {
-          load_b_nk(b, s.K, LDK, 32 * ch + 16, kk, lane);
-          mma_bf16(aK[2], ak, b[0], b[1]);
-          mma_bf16(aK[3], ak, b[2], b[3]);
-          mma_bf16(aQ[2], aq, b[0], b[1]);
-          mma_bf16(aQ[3], aq, b[2], b[3]);
-        }
-      }
-    }
-    GDN_PHASE(2);  // grams
-    // the scaled copies Qt = diag(scale gamma) Q and Kt = diag(e) K
-    __half* Qt = ws.Qt(slot, hv, p.Hv);
-    __half* Kt = ws.Kt(slot, hv, p.Hv);
-    for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-      const int r = i / (DK / 8), sg = i % (DK / 8);
-      *reinterpret_cast<uint4*>(Qt + swz<DK>(r, sg * 8)) =
-          scale_bf16x8_to_f16(&s.Q[r * LDK + sg * 8], p.scale * s.gam[r]);
-      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, sg * 8)) =
-          scale_bf16x8_to_f16(&s.K[r * LDK + sg * 8], s.e[r]);
-    }
-    __syncthreads();  // Q is dead: its storage becomes A
-    GDN_PHASE(3);  // Qt, Kt
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int x = 0; x < 4; x += 2) {
-        const int r = 16 * rb + gq + ((x >> 1) << 3);
-        const int c0 = 32 * ch + 8 * j + 2 * tq;
-        float pv[2], av[2];
-#pragma unroll
-        for (int y = 0; y < 2; ++y) {
-          const int cc = c0 + y;
-          const bool low = r >= cc && r < L;
-          const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
-          av[y] = (low && r > cc) ? s.beta[r] * m * aK[j][x + y] : 0.f;
-          pv[y] = low ? p.scale * m * aQ[j][x + y] : 0.f;
-          s.A[r * LDA + cc] = av[y];
-        }
-        *reinterpret_cast<uint32_t*>(&s.Ah[r * LDC + c0]) = pack_f16(av[0], av[1]);
-        *reinterpret_cast<uint32_t*>(&s.Pst[swz<kC>(r, c0)]) = pack_f16(pv[0], pv[1]);
-      }
-    }
-    fence_proxy_async();  // P staging is read by a bulk store
-  }
+  // ---- #2 grams: one M = 128 MMA chain, [K; Q] K^T -> tensor columns 0-63 ----
+  // One thread spins on each barrier; the others block in bar.sync and then
+  // observe the completed phase with a single test.
+  if (tid == 0 && !mbar_wait(bar_kq, 0, p.err)) *s_abort = 1;
   __syncthreads();
-
-  GDN_PHASE(4);  // masks
-  // ---- #3 Solve and the scaled operands --------------------------------------
-  if (tid == 0) {  // P leaves in one bulk store while the solve runs
+  if (!*s_abort) mbar_wait(bar_kq, 0, p.err);
+  GDN_STAMP(32, 0);  // K, Q landed
+  if (L < kC) {  // ragged chunk: rows past the sequence end are zero
+    for (int i = tid; i < (DK / 64) * 2 * (kC - L) * 8; i += kThreads) {
+      const int ch = i & 7, rr = L + ((i >> 3) % (kC - L)), blk = (i >> 3) / (kC - L);
+      *reinterpret_cast<uint4*>(sm + blk * 8192 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async();
-    bulk_s2g(Pout, s.Pst, kC * kC * 2);
-    bulk_commit();
+    __syncthreads();
   }
-  solve_unit_lower_64(s.A, LDA, s.Ah, s.Tm, LDA, s.Th, LDC);
-  if (tid == 0) bulk_wait_read<0>();
-  __syncthreads();  // P staging is free: Tw takes its place
-  GDN_PHASE(5);  // solve
-  for (int e = tid; e < kC * (kC / 8); e += kThreads) {  // 8 columns per item, 16-byte stores
-    const int r = e >> 3, c0 = (e & 7) * 8;
-    uint4 w, u;
-    __nv_bfloat162* wp = reinterpret_cast<__nv_bfloat162*>(&w);
-    __half2* up = reinterpret_cast<__half2*>(&u);
+  if (tid == 0 && !*s_abort) {
+    constexpr uint32_t idg = idesc_f16(128, 64, true, false, false);
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int cc = c0 + 2 * x;
-      const float t0 = s.Tm[r * LDA + cc], t1 = s.Tm[r * LDA + cc + 1];
-      const float b0 = s.beta[cc], b1 = s.beta[cc + 1];
-      wp[x] = __floats2bfloat162_rn(t0 * b0 * s.gam[cc], t1 * b1 * s.gam[cc + 1]);
-      up[x] = __floats2half2_rn(t0 * b0, t1 * b1);
+    for (int s = 0; s < DK / 16; ++s) {
+      const uint32_t a = sbase + (s >> 2) * 16384 + (s & 3) * 32;
+      tc_mma(tmem, sw128_desc(a, 16, 1024), sw128_desc(a, 16, 1024), idg, s > 0);
     }
-    *reinterpret_cast<uint4*>(&s.Tw[r * LDC + c0]) = w;
-    *reinterpret_cast<uint4*>(&s.Tu[r * LDC + c0]) = u;
+    tc_commit(bar_mma);
   }
-  __syncthreads();
-  GDN_PHASE(6);  // Tw, Tu
-
-  // ---- #4 W = Tw K, U = Tu V (lower-triangular Tw/Tu: k <= row block) -------
+  // meanwhile: the scaled copy Kt = diag(e) K
   {
-    const int rb = warp & 3, nh = warp >> 2;
-    constexpr int WNT = DK / 16, UNT = DV / 16;  // n8 tiles per warp (half the columns)
-    float aW[WNT][4], aU[UNT][4];
+    __half* Kt = ws.Kt(slot, hv, p.Hv);
+    constexpr int kRowChunks = DK / 8;
+    for (int i = tid; i < kC * kRowChunks; i += kThreads) {
+      const int r = i / kRowChunks, ch = i % kRowChunks;
+      const unsigned char* src = sm + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, ch * 8)) = scale_bf16x8_to_f16(src, s_e[r]);
+    }
+  }
+  GDN_STAMP(33, 0);  // Kt written (thread 0's share)
+  if (tid == 0 && !*s_abort) {
+    if (!mbar_wait(bar_mma, 0, p.err)) {
+      *s_abort = 1;
+    } else if (Lo::kVinQ) {  // the grams have read Q: its rows take V
+      mbar_expect_tx(bar_v, (unsigned)kC * DV * 2);
 #pragma unroll
-    for (int j = 0; j < WNT; ++j)
+      for (int vb = 0; vb < DV / 64; ++vb)
+        tma_load_2d(sm + Lo::kV + vb * Lo::kVStride, &tmv, hv * DV + vb * 64, t0, bar_v);
+    }
+  }
+  __syncthreads();  // grams landed
+  if (!*s_abort) mbar_wait(bar_mma, 0, p.err);
+  tc_fence_after();
+  GDN_PHASE(1);  // grams + Kt
+
+  // ---- masks: A (fp16 + fp32 diagonal blocks) and P, from the grams ---------
+  if (!*s_abort) {
+    const int q4 = warp & 3, h = warp >> 2;
+    const int R = 32 * q4 + lane;  // gram row: 0-63 K K^T, 64-127 Q K^T
+    const bool isP = R >= kC;
+    const int r = R & (kC - 1), c0 = 32 * h;
+    float x[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + c0, x);
+    const float Gr = s_G[r], rowf = isP ? p.scale : s_beta[r];
+    const int lim = isP ? r : r - 1;  // last column kept
 #pragma unroll
-      for (int x = 0; x < 4; ++x) aW[j][x] = 0.f;
+    for (int j = 0; j < 32; ++j) {
+      const int cc = c0 + j;
+      const float m = ex2_approx((Gr - s_G[cc]) * kLog2e);
+      x[j] = (cc <= lim && r < L) ? rowf * m * x[j] : 0.f;
+    }
+    if (isP) {
+      __half* P = ws.P(slot, hv, p.Hv);
 #pragma unroll
-    for (int j = 0; j < UNT; ++j)
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(P + swz<kC>(r, c0 + 8 * m)) = pack8_f16(x + 8 * m);
+    } else {
 #pragma unroll
-      for (int x = 0; x < 4; ++x) aU[j][x] = 0.f;
-    for (int kk = 0; kk <= 16 * rb; kk += 16) {
-      uint32_t a[4], b[4];
-      load_a(a, s.Tw, LDC, 16 * rb, kk, lane);
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(Ah + r * kLDH + c0 + 8 * m) = pack8_f16(x + 8 * m);
+      const int b = r >> 4;  // diagonal block of this row, kept in fp32 for the substitution
+      if ((b >> 1) == h) {
+        float4* dst = reinterpret_cast<float4*>(Ad + b * 256 + (r & 15) * 16);
+        const bool hi = b & 1;  // columns 16-31 of this half (selects keep indices static)
 #pragma unroll
-      for (int j = 0; j < WNT; j += 2) {
-        load_b_kn(b, s.K, LDK, nh * (DK / 2) + 8 * j, kk, lane);
-        mma_bf16(aW[j], a, b[0], b[1]);
-        mma_bf16(aW[j + 1], a, b[2], b[3]);
-      }
-      load_a(a, s.Tu, LDC, 16 * rb, kk, lane);
-#pragma unroll
-      for (int j = 0; j < UNT; j += 2) {
-        load_b_kn(b, s.V, LDV, nh * (DV / 2) + 8 * j, kk, lane);
-        mma_f16(aU[j], a, b[0], b[1]);
-        mma_f16(aU[j + 1], a, b[2], b[3]);
+        for (int m = 0; m < 4; ++m)
+          dst[m] = make_float4(hi ? x[16 + 4 * m] : x[4 * m], hi ? x[17 + 4 * m] : x[4 * m + 1],
+                               hi ? x[18 + 4 * m] : x[4 * m + 2], hi ? x[19 + 4 * m] : x[4 * m + 3]);
       }
     }
-    __syncthreads();  // Tm and A/Q storage are dead: stage W and U there
-    const int r0 = 16 * rb + gq;
+  }
+  tc_fence_before();
+  __syncthreads();
+  GDN_PHASE(2);  // masks
+
+  // ---- #3 Solve: Tm = (I + A)^-1, written as Th (fp16), Tw and Tu ------------
+  // Diagonal 16x16 blocks in fp32 (warp b, lane l = column l of block b), by
+  // right-looking substitution: once x_m is final it updates every x_i, i > m,
+  // so the dependent chain is 15 FMAs deep.  Warps 4-7 zero the strictly upper
+  // blocks meanwhile.
+  if (!*s_abort) {
+    if (warp < 4) {
+      if (lane < 16) {
+        const int b = warp, l = lane;
+        const float* Ab = Ad + b * 256;
+        float x[16];
 #pragma unroll
-    for (int j = 0; j < WNT; ++j) {
-      const int col = nh * (DK / 2) + 8 * j + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&s.Wst[r0 * LDK + col]) = pack_f16(aW[j][0], aW[j][1]);
-      *reinterpret_cast<uint32_t*>(&s.Wst[(r0 + 8) * LDK + col]) = pack_f16(aW[j][2], aW[j][3]);
-    }
+        for (int i = 0; i < 16; ++i) x[i] = (i == l) ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < UNT; ++j) {
-      const int col = nh * (DV / 2) + 8 * j + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&s.Ust[r0 * LDV + col]) = pack_f16(aU[j][0], aU[j][1]);
-      *reinterpret_cast<uint32_t*>(&s.Ust[(r0 + 8) * LDV + col]) = pack_f16(aU[j][2], aU[j][3]);
+        for (int m = 0; m < 15; ++m)
+#pragma unroll
+          for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Ab[i * 16 + m], x[m], x[i]);
+        const int cc = 16 * b + l;
+        const float fw = s_bg[cc], fu = s_beta[cc];
+        __nv_bfloat16* Twb = reinterpret_cast<__nv_bfloat16*>(Tw);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int rr = 16 * b + i;
+          Th[rr * kLDH + cc] = __float2half_rn(x[i]);
+          Twb[sw128(rr, cc)] = __float2bfloat16_rn(x[i] * fw);
+          Tu[sw128(rr, cc)] = __float2half_rn(x[i] * fu);
+        }
+      }
+    } else {
+      for (int e = tid - 128; e < kC * 8; e += 128) {  // 16-byte chunks of the upper blocks
+        const int rr = e >> 3, ch = e & 7;
+        if ((ch >> 1) > (rr >> 4)) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&Th[rr * kLDH + 8 * ch]) = z;
+          *reinterpret_cast<uint4*>(&Tw[sw128(rr, 8 * ch)]) = z;
+          *reinterpret_cast<uint4*>(&Tu[sw128(rr, 8 * ch)]) = z;
+        }
+      }
     }
   }
   __syncthreads();
-  GDN_PHASE(7);  // W/U products
-  __half* Wout = ws.W(slot, hv, p.Hv);
-  __half* Uout = ws.U(slot, hv, p.Hv);
-  for (int i = tid; i < kC * (DK / 8); i += kThreads) {
-    const int r = i / (DK / 8), sg = i % (DK / 8);
-    *reinterpret_cast<uint4*>(Wout + swz<DK>(r, sg * 8)) =
-        *reinterpret_cast<const uint4*>(&s.Wst[r * LDK + sg * 8]);
+  GDN_STAMP(34, 0);  // diagonal blocks done
+  GDN_STAMP(40, 128);
+  if (!*s_abort) {
+    if (warp < 2) {
+      // level 1: T10 = -(T11 A10) T00 (warp 0), T32 = -(T33 A32) T22 (warp 1)
+      {
+        const int i0 = 16 + 32 * warp, j0 = 32 * warp;
+        float y[2][4] = {}, t[2][4] = {};
+        uint32_t a[4], b[4];
+        load_a(a, Th, kLDH, i0, i0, lane);     // T_II
+        load_b_kn(b, Ah, kLDH, j0, i0, lane);  // A_IJ as [k][n]
+        mma_f16(y[0], a, b[0], b[1]);
+        mma_f16(y[1], a, b[2], b[3]);
+        c_to_a(a, y[0], y[1]);
+        load_b_kn(b, Th, kLDH, j0, j0, lane);  // T_JJ as [k][n]
+        mma_f16(t[0], a, b[0], b[1]);
+        mma_f16(t[1], a, b[2], b[3]);
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+          for (int xh = 0; xh < 2; ++xh) {
+            const int rr = i0 + gq + 8 * xh, cc = j0 + 8 * jn + 2 * tq;
+            put_t2(Th, Tw, Tu, s_bg, s_beta, rr, cc, -t[jn][2 * xh], -t[jn][2 * xh + 1]);
+          }
+      }
+      named_sync(1, 64);
+      // level 2: rows 32..63 x columns 0..31 = -(T_BB A_BA) T_AA; warp w takes 16 rows
+      {
+        const int i0 = 32 + 16 * warp;
+        float y[4][4] = {}, t[4][4] = {};
+        uint32_t a[4], b[4];
+        for (int k0 = 32; k0 <= i0; k0 += 16) {  // T_BB is lower triangular
+          load_a(a, Th, kLDH, i0, k0, lane);
+          load_b_kn(b, Ah, kLDH, 0, k0, lane);
+          mma_f16(y[0], a, b[0], b[1]);
+          mma_f16(y[1], a, b[2], b[3]);
+          load_b_kn(b, Ah, kLDH, 16, k0, lane);
+          mma_f16(y[2], a, b[0], b[1]);
+          mma_f16(y[3], a, b[2], b[3]);
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {  // k over the 32 columns of Y
+          c_to_a(a, y[2 * s], y[2 * s + 1]);
+          load_b_kn(b, Th, kLDH, 0, 16 * s, lane);
+          mma_f16(t[0], a, b[0], b[1]);
+          mma_f16(t[1], a, b[2], b[3]);
+          load_b_kn(b, Th, kLDH, 16, 16 * s, lane);
+          mma_f16(t[2], a, b[0], b[1]);
+          mma_f16(t[3], a, b[2], b[3]);
+        }
+#pragma unroll
+        for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+          for (int xh = 0; xh < 2; ++xh) {
+            const int rr = i0 + gq + 8 * xh, cc = 8 * jn + 2 * tq;
+            put_t2(nullptr, Tw, Tu, s_bg, s_beta, rr, cc, -t[jn][2 * xh], -t[jn][2 * xh + 1]);
+          }
+      }
+      GDN_STAMP(35, 0);  // merges done
+    } else if (warp >= 4) {
+      // meanwhile: V lands; zero its rows past the sequence end, rewrite it as fp16
+      if (tid == 128 && !mbar_wait(bar_v, 0, p.err)) *s_abort = 1;
+      named_sync(2, 128);
+      if (!*s_abort) mbar_wait(bar_v, 0, p.err);
+      GDN_STAMP(41, 128);  // V landed
+      for (int i = tid - 128; i < (DV / 64) * kC * 8; i += 128) {
+        const int ch = i & 7, rr = (i >> 3) & (kC - 1), vb = i >> 9;
+        unsigned char* q = sm + Lo::kV + vb * Lo::kVStride + rr * 128 + ch * 16;
+        if (rr >= L) *reinterpret_cast<uint4*>(q) = make_uint4(0, 0, 0, 0);
+        else bf16x8_to_f16x8(q);
+      }
+      GDN_STAMP(42, 128);  // V converted
+    }
   }
-  const int dvt = ws.dvt;
-  for (int i = tid; i < kC * (DV / 8); i += kThreads) {  // U tile-major: [dv/t][64][t]
-    const int r = i / (DV / 8), sg = i % (DV / 8);
-    const int col = sg * 8, t = col / dvt, w = col % dvt;
-    *reinterpret_cast<uint4*>(Uout + (t * kC + r) * dvt + w) =
-        *reinterpret_cast<const uint4*>(&s.Ust[r * LDV + col]);
+  fence_proxy_async();  // Tw, Tu and V are read by the tensor cores next
+  tc_fence_before();
+  __syncthreads();
+  GDN_PHASE(3);  // solve (+ V)
+
+  // ---- #4 W^T = K^T Tw^T (bf16, columns 64-127), U^T = V^T Tu^T (fp16, 0-63)
+  if (tid == 0 && !*s_abort) {
+    tc_fence_after();
+    constexpr uint32_t idw = idesc_f16(DK, 64, true, true, false);
+    constexpr uint32_t idu = idesc_f16(DV, 64, false, true, false);
+#pragma unroll
+    for (int s = 0; s < kC / 16; ++s)
+      tc_mma(tmem + 64, sw128_desc(sbase + s * 2048, 16384, 1024),
+             sw128_desc(sbase + Lo::kTw + s * 32, 16, 1024), idw, s > 0);
+#pragma unroll
+    for (int s = 0; s < kC / 16; ++s)
+      tc_mma(tmem, sw128_desc(sbase + Lo::kV + s * 2048, Lo::kVStride, 1024),
+             sw128_desc(sbase + Lo::kTu + s * 32, 16, 1024), idu, s > 0);
+    tc_commit(bar_mma);
   }
-  GDN_PHASE(8);  // W/U stores
+  if (tid == 0 && !*s_abort && !mbar_wait(bar_mma, 1, p.err)) *s_abort = 1;
+  __syncthreads();
+  if (!*s_abort) mbar_wait(bar_mma, 1, p.err);
+  GDN_STAMP(36, 0);  // W, U products landed
+  tc_fence_after();
+  if (!*s_abort) {
+    // tensor-memory lane -> d: lane d for M = 128; rows 16q + i sit in lanes 32q + i for M = 64
+    const int q4 = warp & 3, h = warp >> 2;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+    float x[32];
+    tmem_ld32(lane_base + 64 + 32 * h, x);
+    if (DK == 128 || lane < 16) {
+      const int d = DK == 128 ? 32 * q4 + lane : 16 * q4 + lane;
+      __half* Wt = ws.W(slot, hv, p.Hv);  // [dk][64], swz<64>
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(Wt + swz<kC>(d, 32 * h + 8 * m)) = pack8_f16(x + 8 * m);
+    }
+    tmem_ld32(lane_base + 32 * h, x);
+    if (DV == 128 || lane < 16) {
+      const int d = DV == 128 ? 32 * q4 + lane : 16 * q4 + lane;
+      __half* Ut = ws.U(slot, hv, p.Hv);  // [dv][64], plain
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *reinterpret_cast<uint4*>(Ut + d * kC + 32 * h + 8 * m) = pack8_f16(x + 8 * m);
+    }
+  }
+  GDN_PHASE(4);  // W/U
+  GDN_STAMP(37, 0);  // W, U stored
+  // ---- teardown: after an expired wait, let copies in flight land first ------
+  if (*s_abort && tid == 0) {
+    mbar_wait(bar_kq, 0, nullptr);
+    mbar_wait(bar_v, 0, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
 }
+
+// ---- host: tensor maps -------------------------------------------------------
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_fn() {
+  static const EncodeTiled fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 template <int DK, int DV>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
-  const size_t smem = sizeof(PrepSmem<DK, DV>);
+  using Lo = PrepLayout<DK, DV>;
+  const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
+  CUtensorMap mq, mk, mv;
+  if (!make_tensor_map_bf16(&mq, p.q, rows, (long long)p.Hqk * DK) ||
+      !make_tensor_map_bf16(&mk, p.k, rows, (long long)p.Hqk * DK) ||
+      !make_tensor_map_bf16(&mv, p.v, rows, (long long)p.Hv * DV))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK, DV>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gdn_prep_kernel<DK, DV>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   const long long grid = ws.n_slots * p.Hv;
-  gdn_prep_kernel<DK, DV><<<(unsigned)grid, kThreads, smem, stream>>>(p, ws);
+  gdn_prep_kernel<DK, DV><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq, mk, mv);
   return cudaGetLastError();
 }
 

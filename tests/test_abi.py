@@ -123,9 +123,11 @@ def test_product_path_does_not_import_the_oracle():
 
 
 def test_workspace_size_formula(lib):
-    # record: W, Kt, Qt [64][dk], P [64][64], U [64][dv], 16 B, H [dk][dv], Vn [64][dv] (fp16)
+    # record: W^T [dk][64], Kt [64][dk], P [64][64], U^T [dv][64] (fp16), 68 fp32
+    # gate factors, padded to a 128-byte multiple
     def rec(dk, dv):
-        return 3 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 16 + dk * dv * 2 + 64 * dv * 2
+        raw = 2 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 68 * 4
+        return (raw + 127) // 128 * 128
     # fixed-length rows: N * ceil(T/64) slots x Hv records
     assert lib.gdn_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == 64 * 16 * rec(128, 128)
     assert lib.gdn_chunk_fwd_workspace_size(2, 100, 1, 4, 128, 64, 64, 0) == 2 * 2 * 4 * rec(128, 64)
