@@ -45,7 +45,11 @@ from linear_attention_prefill_gb300.workloads import HEADLINE, WORKLOADS, make_d
 METRIC = "GDN chunked-prefill tokens/s per layer on 1 GB300; % of TC/HBM roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 320 * 2 ** 20
-KERNEL_NAME = "gdn_fwd_bf16_kernel"
+# One gdn_chunk_fwd call is two launches on the caller's stream (the chunk-parallel
+# prep kernel, then the chunk-serial chain kernel that also writes o); the roofline
+# block times the call, and the launch list in profiles/ gives each kernel's share.
+KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
+LAUNCHES_PER_CALL = 2
 
 
 def kernel_source_hash() -> str:
@@ -60,7 +64,8 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on this exact source."""
+    """DRAM bytes (read + write) per forward call, summed over its launches, from a
+    committed ncu capture - only if it was taken on this exact kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -69,7 +74,7 @@ def measured_traffic(workload: str):
         return None
     if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec.get("dram_bytes_per_call")
 
 
 def config_of(w, world, extra=None):
@@ -270,7 +275,7 @@ def bench_cuda(args, w, rank, world, local_rank):
     local_ms = sum(ms)
     job_ms, job_tokens = reduce_timing(local_ms, float(w.T_total * args.steps))
     value = job_tokens / (job_ms / 1e3)
-    launches = args.steps  # one gdn_fwd kernel per step
+    launches = LAUNCHES_PER_CALL * args.steps
 
     # end to end through the public API from pinned host memory
     host = {k_: (None if x[k_] is None else x[k_].detach().cpu().pin_memory())

@@ -45,7 +45,7 @@ typedef struct CUstream_st* gdn_stream_t; /* ABI-identical to cudaStream_t */
 typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, misaligned pointer, Hv % Hqk != 0 */
-  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: dk, dv not in {64, 128}; chunk != 64 */
+  GDN_ERR_UNSUPPORTED = 2, /* valid but not built: dk, dv or chunk not in {64, 128} */
   GDN_ERR_CUDA = 3,        /* a CUDA call failed (launch error, no device) */
   GDN_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see gdn_device_status) */
 } gdn_status;
@@ -66,8 +66,11 @@ typedef enum {
  *          T tokens; with cu_seqlens it is one packed row of T tokens.
  *   T      tokens per row (packed total with cu_seqlens); T = 0 is a no-op
  *          that copies h0 (or zeros) to hT
- *   chunk  chunk length C of the chunkwise form (64); chunks restart at
- *          every sequence start, the last one may be partial
+ *   chunk  chunk length C of the chunkwise form, 64 or 128; chunks restart
+ *          at every sequence start, the last one may be partial.  The chunked
+ *          recurrence gives the same o and hT for any C (it is exact, not an
+ *          approximation), so a 128-token chunk is computed as two 64-token
+ *          chunks: both values give identical results and timings here.
  *   scale  multiplies q (o_t = S_t (scale q_t)), usually dk^-0.5
  *   cu_seqlens  NULL, or DEVICE int32 [B + 1]: 0 = cu[0] <= cu[1] <= ... <=
  *          cu[B] = T (not checked on the host; empty sequences allowed)
@@ -82,12 +85,11 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
 /*
  * gdn_chunk_fwd_workspace_size - bytes of device workspace gdn_chunk_fwd_ex
  * needs for these sizes (has_cu_seqlens: 1 if cu_seqlens will be passed).
- * The bf16 forward runs in three launches: the chunk-parallel operators #1-#4
- * (Gate, KKT, Solve, W/U) write a per-(chunk, v head) record (W, diag(e) K,
- * diag(scale gamma) Q, P, U: fp16), the chunk-serial #5 H launch adds the state
- * entering each chunk and V_new, and the chunk-parallel #6 O launch reads them:
- * 120 KB per chunk and v head at d = 128.  Returns 0 for sizes gdn_chunk_fwd
- * would reject.
+ * The bf16 forward runs in two launches: the chunk-parallel operators #1-#4
+ * (Gate, KKT, Solve, W/U) write one record per (64-token chunk, v head) -
+ * W^T, diag(e) K, P and U^T in fp16 plus the gate factors, 57.7 KB at
+ * d = 128 - and the chunk-serial launch (#5 H with #6 O) reads them.  Returns 0
+ * for sizes gdn_chunk_fwd would reject.
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
                                     int has_cu_seqlens);
@@ -115,7 +117,7 @@ gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const f
  * synchronisation an allocation can imply, or code embedded in a runtime that
  * owns all device memory through its own pool.
  *  - Limit: gdn_chunk_fwd_workspace_size(...) must be at most 32 MiB (about
- *    270 chunk-and-v-head records at dk = dv = 128, e.g. 4096 tokens x 4 v
+ *    580 chunk-and-v-head records at dk = dv = 128, e.g. 4096 tokens x 9 v
  *    heads); larger sizes return GDN_ERR_INVALID_ARG and launch nothing.
  *  - Every GPU that runs the library's device code keeps those 32 MiB until
  *    the process exits.

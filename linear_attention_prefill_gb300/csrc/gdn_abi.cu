@@ -64,7 +64,8 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv=%d is not a multiple of Hqk=%d", Hv, Hqk);
   if (!head_dim_ok(dk) || !head_dim_ok(dv))
     return fail(GDN_ERR_UNSUPPORTED, "dk=%d, dv=%d: supported head dims are 64 and 128", dk, dv);
-  if (chunk != 64) return fail(GDN_ERR_UNSUPPORTED, "chunk=%d: supported chunk is 64", chunk);
+  if (chunk != 64 && chunk != 128)
+    return fail(GDN_ERR_UNSUPPORTED, "chunk=%d: supported chunk lengths are 64 and 128", chunk);
   if (!(scale == scale)) return fail(GDN_ERR_INVALID_ARG, "scale is NaN");
   if (cu_seqlens && B < 1) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B >= 1 sequences");
   const long long rows = cu_seqlens ? 1 : (long long)B;

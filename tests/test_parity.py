@@ -145,6 +145,18 @@ def test_decay_regimes(cuda_lib, dtype, decay):
     check_heads(x, o, hT, heads=range(2), dtype=dtype)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_chunk_128_is_the_same_function(cuda_lib, dtype):
+    """chunk = 128 runs as two 64-token chunks: bit-identical to chunk = 64, and the
+    oracle's own 128-token chunked form agrees with its recurrence."""
+    w = small(0, Hqk=1, Hv=2, seqlens=[300, 0, 129], dtype=dtype, seed=19)
+    x = make_inputs(w, device="cuda")
+    o64, h64 = run(cuda_lib, x, chunk=64)
+    o128, h128 = run(cuda_lib, x, chunk=128)
+    assert torch.equal(o64, o128) and torch.equal(h64, h128)
+    check_heads(x, o128, h128, heads=range(2), dtype=dtype)
+
+
 def test_unsupported_chunk_is_reported(cuda_lib):
     w = small(64, seed=17)
     x = make_inputs(w, device="cuda")
