@@ -87,7 +87,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;  // 4 chain + 4 output warp arrivals: stage consumed
   uint64_t* pub = empty + kStages;   // chain -> output: H[b], Vn[b] ready
   uint64_t* pubd = pub + kPub;       // output -> chain: H[b], Vn[b] consumed (4 arrivals)
-  volatile int* s_abort = reinterpret_cast<volatile int*>(pubd + kPub);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(pubd + kPub);  // any wait expired
+  // the chain warps' stop decision: written by thread 0 before a named barrier and
+  // read by all four warps after it, so they never split at a barrier
+  volatile int* s_cstop = s_abort + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pubd[i], 4);
     }
     *s_abort = 0;
+    *s_cstop = 0;
     mbar_fence_init();
   }
 
@@ -302,9 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pack_f16(u1.x - wh[0][j][2] - wh[1][j][2], u1.y - wh[0][j][3] - wh[1][j][3]);
       }
     }
+    if (tid == 0) *s_cstop = *s_abort;
     named_sync(1, kComputeThreads);  // V_new complete (H[hb] was complete before)
     GDN_PHASE(20);  // V_new
-    if (*s_abort) break;
+    if (*s_cstop) break;
     if (tid == 0) mbar_arrive(&pub[hb]);
 
     // #5 update: h = gamma_last h + Kt^T V_new, written straight into H[hn]

@@ -19,9 +19,10 @@
 // gamma))^T, and V (loaded into the Q rows once Q is consumed) that of U^T:
 // the products come out transposed, one d index per tensor-memory lane, so each
 // thread writes whole 16-byte row segments of W^T and U^T.  Accumulators stay
-// in 128 tensor-memory columns and shared memory in ~72 KB, so three tasks
-// share an SM.  The triangular solve keeps its fp32 diagonal blocks and fp16
-// mma.sync merges, and writes the scaled MMA operands directly.
+// in 128 tensor-memory columns and shared memory in ~54 KB (the Q rows hold the
+// solve's fp16 tiles, then V), so four tasks share an SM.  The triangular solve
+// keeps its fp32 diagonal blocks and fp16 mma.sync merges, and writes the
+// scaled MMA operands directly.
 //
 // Precision: products accumulate in fp32.  The grams and W take the bf16
 // inputs as they are (W's left factor rounded to bf16: its share of the error
@@ -38,28 +39,31 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kThreads = 256;
-constexpr int kLDH = kC + 8;  // fp16 row stride of Ah and Th (conflict-free ldmatrix)
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared-memory map (byte offsets from a 1024-aligned base).
+// Shared-memory map (byte offsets from a 1024-aligned base), ~54 KB at d = 128
+// so that four tasks share an SM.  The Q rows are reused twice: once the grams
+// have read Q they hold the solve's fp16 copies Ah and Th, and once the solve
+// is done they take V.
 template <int DK, int DV>
 struct PrepLayout {
   // [DK/64][128 rows][64] bf16, 128-byte swizzle: rows 0-63 K, rows 64-127 Q
   static constexpr int kKQBytes = (DK / 64) * 16384;
-  // V takes the Q rows once the grams are done (when it fits there)
-  static constexpr bool kVinQ = DV <= DK;
-  static constexpr int kV = kVinQ ? 8192 : kKQBytes;
+  static constexpr bool kThInQ = DK == 128;             // Th in the second block's Q rows
+  static constexpr bool kVinQ = DV <= DK;               // V in the Q rows after the solve
+  static constexpr int kAh = 8192;                      // fp16 [64][64] swz<64>, first Q rows
+  static constexpr int kTh = kThInQ ? 24576 : kKQBytes; // fp16 [64][64] swz<64>
+  static constexpr int kAfterTh = kKQBytes + (kThInQ ? 0 : 8192);
+  static constexpr int kV = kVinQ ? 8192 : kAfterTh;
   static constexpr int kVStride = kVinQ ? 16384 : 8192;  // bytes between 64-column blocks
-  static constexpr int kTw = kKQBytes + (kVinQ ? 0 : (DV / 64) * 8192);  // bf16 [64][64] sw128
+  static constexpr int kTw = kAfterTh + (kVinQ ? 0 : (DV / 64) * 8192);  // bf16 [64][64] sw128
   static constexpr int kTu = kTw + 8192;                                   // fp16 [64][64] sw128
-  static constexpr int kAh = kTu + 8192;                                   // fp16 [64][kLDH]
-  static constexpr int kTh = kAh + kC * kLDH * 2;                          // fp16 [64][kLDH]
-  static constexpr int kAd = kTh + kC * kLDH * 2;      // fp32 diagonal blocks of A [4][16][16]
+  static constexpr int kAd = kTu + 8192;               // fp32 diagonal blocks of A [4][16][16]
   static constexpr int kVec = kAd + 4 * 256 * 4;       // beta, G, gamma, e, beta*gamma [5][64]
-  static constexpr int kBar = kVec + 5 * kC * 4;       // 3 mbarriers, tmem address, abort flag
+  static constexpr int kBar = kVec + 5 * kC * 4;       // 5 mbarriers, tmem address, abort flag
   static constexpr int kBytes = kBar + 64;
   static constexpr int kAlloc = kBytes + 1024;         // slack to align the base
-  static_assert(kTw % 1024 == 0 && kAh % 16 == 0 && kAd % 16 == 0, "alignment");
+  static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kAd % 16 == 0, "alignment");
 };
 
 // 8 bf16 values at p (16-byte aligned) times `scale`, rounded once to fp16.
@@ -86,13 +90,13 @@ __device__ __forceinline__ uint4 pack8_f16(const float* x) {
 // Tu = T diag(beta) (fp16).
 __device__ __forceinline__ void put_t2(__half* Th, __half* Tw, __half* Tu, const float* bg,
                                        const float* beta, int r, int c, float t0, float t1) {
-  if (Th) *reinterpret_cast<uint32_t*>(&Th[r * kLDH + c]) = pack_f16(t0, t1);
+  if (Th) *reinterpret_cast<uint32_t*>(&Th[swz<kC>(r, c)]) = pack_f16(t0, t1);
   *reinterpret_cast<uint32_t*>(&Tw[sw128(r, c)]) = pack_bf16(t0 * bg[c], t1 * bg[c + 1]);
   *reinterpret_cast<uint32_t*>(&Tu[sw128(r, c)]) = pack_f16(t0 * beta[c], t1 * beta[c + 1]);
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, 4)
     gdn_prep_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using Lo = PrepLayout<DK, DV>;
@@ -112,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 3)
   float* s_bg = s_e + kC;
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + Lo::kBar);
   uint64_t* bar_v = bar_kq + 1;
-  uint64_t* bar_mma = bar_kq + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kq + 3);
+  uint64_t* bar_mma = bar_kq + 2;  // grams
+  uint64_t* bar_w = bar_kq + 3;    // W^T product
+  uint64_t* bar_u = bar_kq + 4;    // U^T product
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bar_kq + 5);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -137,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     mbar_init(bar_kq, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_w, 1);
+    mbar_init(bar_u, 1);
     *s_abort = 0;
     mbar_fence_init();
     mbar_expect_tx(bar_kq, 2u * kC * DK * 2);
@@ -230,17 +238,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   GDN_STAMP(33, 0);  // Kt written (thread 0's share)
-  if (tid == 0 && !*s_abort) {
-    if (!mbar_wait(bar_mma, 0, p.err)) {
-      *s_abort = 1;
-    } else if (Lo::kVinQ) {  // the grams have read Q: its rows take V
-      mbar_expect_tx(bar_v, (unsigned)kC * DV * 2);
-#pragma unroll
-      for (int vb = 0; vb < DV / 64; ++vb)
-        tma_load_2d(sm + Lo::kV + vb * Lo::kVStride, &tmv, hv * DV + vb * 64, t0, bar_v);
-    }
-  }
-  __syncthreads();  // grams landed
+  if (tid == 0 && !*s_abort && !mbar_wait(bar_mma, 0, p.err)) *s_abort = 1;
+  __syncthreads();  // grams landed: the Q rows are free for Ah and Th
   if (!*s_abort) mbar_wait(bar_mma, 0, p.err);
   tc_fence_after();
   GDN_PHASE(1);  // grams + Kt
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     } else {
 #pragma unroll
       for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<uint4*>(Ah + r * kLDH + c0 + 8 * m) = pack8_f16(x + 8 * m);
+        *reinterpret_cast<uint4*>(Ah + swz<kC>(r, c0 + 8 * m)) = pack8_f16(x + 8 * m);
       const int b = r >> 4;  // diagonal block of this row, kept in fp32 for the substitution
       if ((b >> 1) == h) {
         float4* dst = reinterpret_cast<float4*>(Ad + b * 256 + (r & 15) * 16);
@@ -308,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int rr = 16 * b + i;
-          Th[rr * kLDH + cc] = __float2half_rn(x[i]);
+          Th[swz<kC>(rr, cc)] = __float2half_rn(x[i]);
           Twb[sw128(rr, cc)] = __float2bfloat16_rn(x[i] * fw);
           Tu[sw128(rr, cc)] = __float2half_rn(x[i] * fu);
         }
@@ -318,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int rr = e >> 3, ch = e & 7;
         if ((ch >> 1) > (rr >> 4)) {
           const uint4 z = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(&Th[rr * kLDH + 8 * ch]) = z;
+          *reinterpret_cast<uint4*>(&Th[swz<kC>(rr, 8 * ch)]) = z;
           *reinterpret_cast<uint4*>(&Tw[sw128(rr, 8 * ch)]) = z;
           *reinterpret_cast<uint4*>(&Tu[sw128(rr, 8 * ch)]) = z;
         }
@@ -335,12 +334,12 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int i0 = 16 + 32 * warp, j0 = 32 * warp;
         float y[2][4] = {}, t[2][4] = {};
         uint32_t a[4], b[4];
-        load_a(a, Th, kLDH, i0, i0, lane);     // T_II
-        load_b_kn(b, Ah, kLDH, j0, i0, lane);  // A_IJ as [k][n]
+        load_a_sw<kC>(a, Th, i0, i0, lane);     // T_II
+        load_b_kn_sw<kC>(b, Ah, j0, i0, lane);  // A_IJ as [k][n]
         mma_f16(y[0], a, b[0], b[1]);
         mma_f16(y[1], a, b[2], b[3]);
         c_to_a(a, y[0], y[1]);
-        load_b_kn(b, Th, kLDH, j0, j0, lane);  // T_JJ as [k][n]
+        load_b_kn_sw<kC>(b, Th, j0, j0, lane);  // T_JJ as [k][n]
         mma_f16(t[0], a, b[0], b[1]);
         mma_f16(t[1], a, b[2], b[3]);
 #pragma unroll
@@ -358,21 +357,21 @@ __global__ void __launch_bounds__(kThreads, 3)
         float y[4][4] = {}, t[4][4] = {};
         uint32_t a[4], b[4];
         for (int k0 = 32; k0 <= i0; k0 += 16) {  // T_BB is lower triangular
-          load_a(a, Th, kLDH, i0, k0, lane);
-          load_b_kn(b, Ah, kLDH, 0, k0, lane);
+          load_a_sw<kC>(a, Th, i0, k0, lane);
+          load_b_kn_sw<kC>(b, Ah, 0, k0, lane);
           mma_f16(y[0], a, b[0], b[1]);
           mma_f16(y[1], a, b[2], b[3]);
-          load_b_kn(b, Ah, kLDH, 16, k0, lane);
+          load_b_kn_sw<kC>(b, Ah, 16, k0, lane);
           mma_f16(y[2], a, b[0], b[1]);
           mma_f16(y[3], a, b[2], b[3]);
         }
 #pragma unroll
         for (int s = 0; s < 2; ++s) {  // k over the 32 columns of Y
           c_to_a(a, y[2 * s], y[2 * s + 1]);
-          load_b_kn(b, Th, kLDH, 0, 16 * s, lane);
+          load_b_kn_sw<kC>(b, Th, 0, 16 * s, lane);
           mma_f16(t[0], a, b[0], b[1]);
           mma_f16(t[1], a, b[2], b[3]);
-          load_b_kn(b, Th, kLDH, 16, 16 * s, lane);
+          load_b_kn_sw<kC>(b, Th, 16, 16 * s, lane);
           mma_f16(t[2], a, b[0], b[1]);
           mma_f16(t[3], a, b[2], b[3]);
         }
@@ -385,50 +384,38 @@ __global__ void __launch_bounds__(kThreads, 3)
           }
       }
       GDN_STAMP(35, 0);  // merges done
-    } else if (warp >= 4) {
-      // meanwhile: V lands; zero its rows past the sequence end, rewrite it as fp16
-      if (tid == 128 && !mbar_wait(bar_v, 0, p.err)) *s_abort = 1;
-      named_sync(2, 128);
-      if (!*s_abort) mbar_wait(bar_v, 0, p.err);
-      GDN_STAMP(41, 128);  // V landed
-      for (int i = tid - 128; i < (DV / 64) * kC * 8; i += 128) {
-        const int ch = i & 7, rr = (i >> 3) & (kC - 1), vb = i >> 9;
-        unsigned char* q = sm + Lo::kV + vb * Lo::kVStride + rr * 128 + ch * 16;
-        if (rr >= L) *reinterpret_cast<uint4*>(q) = make_uint4(0, 0, 0, 0);
-        else bf16x8_to_f16x8(q);
-      }
-      GDN_STAMP(42, 128);  // V converted
     }
   }
-  fence_proxy_async();  // Tw, Tu and V are read by the tensor cores next
+  fence_proxy_async();  // Tw, Tu are read by the tensor cores; the Q rows take V next
   tc_fence_before();
-  __syncthreads();
-  GDN_PHASE(3);  // solve (+ V)
+  __syncthreads();  // the solve is done: Ah and Th are dead
+  GDN_PHASE(3);  // solve
 
-  // ---- #4 W^T = K^T Tw^T (bf16, columns 64-127), U^T = V^T Tu^T (fp16, 0-63)
+  // ---- #4 W^T = K^T Tw^T (bf16, tensor columns 64-127) while V lands in the Q
+  // rows; then U^T = V^T Tu^T (fp16, columns 0-63) -------------------------------
   if (tid == 0 && !*s_abort) {
+    if (Lo::kVinQ) {
+      mbar_expect_tx(bar_v, (unsigned)kC * DV * 2);
+#pragma unroll
+      for (int vb = 0; vb < DV / 64; ++vb)
+        tma_load_2d(sm + Lo::kV + vb * Lo::kVStride, &tmv, hv * DV + vb * 64, t0, bar_v);
+    }
     tc_fence_after();
     constexpr uint32_t idw = idesc_f16(DK, 64, true, true, false);
-    constexpr uint32_t idu = idesc_f16(DV, 64, false, true, false);
 #pragma unroll
     for (int s = 0; s < kC / 16; ++s)
       tc_mma(tmem + 64, sw128_desc(sbase + s * 2048, 16384, 1024),
              sw128_desc(sbase + Lo::kTw + s * 32, 16, 1024), idw, s > 0);
-#pragma unroll
-    for (int s = 0; s < kC / 16; ++s)
-      tc_mma(tmem, sw128_desc(sbase + Lo::kV + s * 2048, Lo::kVStride, 1024),
-             sw128_desc(sbase + Lo::kTu + s * 32, 16, 1024), idu, s > 0);
-    tc_commit(bar_mma);
+    tc_commit(bar_w);
   }
-  if (tid == 0 && !*s_abort && !mbar_wait(bar_mma, 1, p.err)) *s_abort = 1;
+  // tensor-memory lane -> d: lane d for M = 128; rows 16q + i sit in lanes 32q + i for M = 64
+  const int q4 = warp & 3, h = warp >> 2;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+  if (tid == 0 && !*s_abort && !mbar_wait(bar_w, 0, p.err)) *s_abort = 1;
   __syncthreads();
-  if (!*s_abort) mbar_wait(bar_mma, 1, p.err);
-  GDN_STAMP(36, 0);  // W, U products landed
-  tc_fence_after();
   if (!*s_abort) {
-    // tensor-memory lane -> d: lane d for M = 128; rows 16q + i sit in lanes 32q + i for M = 64
-    const int q4 = warp & 3, h = warp >> 2;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+    mbar_wait(bar_w, 0, p.err);
+    tc_fence_after();
     float x[32];
     tmem_ld32(lane_base + 64 + 32 * h, x);
     if (DK == 128 || lane < 16) {
@@ -438,6 +425,38 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int m = 0; m < 4; ++m)
         *reinterpret_cast<uint4*>(Wt + swz<kC>(d, 32 * h + 8 * m)) = pack8_f16(x + 8 * m);
     }
+  }
+  GDN_STAMP(36, 0);  // W stored
+  // V: zero its rows past the sequence end, rewrite it as fp16 for the U product
+  if (tid == 0 && !*s_abort && !mbar_wait(bar_v, 0, p.err)) *s_abort = 1;
+  __syncthreads();
+  if (!*s_abort) {
+    mbar_wait(bar_v, 0, p.err);
+    for (int i = tid; i < (DV / 64) * kC * 8; i += kThreads) {
+      const int ch = i & 7, rr = (i >> 3) & (kC - 1), vb = i >> 9;
+      unsigned char* q = sm + Lo::kV + vb * Lo::kVStride + rr * 128 + ch * 16;
+      if (rr >= L) *reinterpret_cast<uint4*>(q) = make_uint4(0, 0, 0, 0);
+      else bf16x8_to_f16x8(q);
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && !*s_abort) {
+    tc_fence_after();
+    constexpr uint32_t idu = idesc_f16(DV, 64, false, true, false);
+#pragma unroll
+    for (int s = 0; s < kC / 16; ++s)
+      tc_mma(tmem, sw128_desc(sbase + Lo::kV + s * 2048, Lo::kVStride, 1024),
+             sw128_desc(sbase + Lo::kTu + s * 32, 16, 1024), idu, s > 0);
+    tc_commit(bar_u);
+  }
+  if (tid == 0 && !*s_abort && !mbar_wait(bar_u, 0, p.err)) *s_abort = 1;
+  __syncthreads();
+  if (!*s_abort) {
+    mbar_wait(bar_u, 0, p.err);
+    tc_fence_after();
+    float x[32];
     tmem_ld32(lane_base + 32 * h, x);
     if (DV == 128 || lane < 16) {
       const int d = DV == 128 ? 32 * q4 + lane : 16 * q4 + lane;
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   GDN_PHASE(4);  // W/U
   GDN_STAMP(37, 0);  // W, U stored
   // ---- teardown: after an expired wait, let copies in flight land first ------
-  if (*s_abort && tid == 0) {
+  if (*s_abort && tid == 0) {  // bounded: a copy never issued just times out
     mbar_wait(bar_kq, 0, nullptr);
     mbar_wait(bar_v, 0, nullptr);
   }
