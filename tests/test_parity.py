@@ -145,6 +145,15 @@ def test_decay_regimes(cuda_lib, dtype, decay):
     check_heads(x, o, hT, heads=range(2), dtype=dtype)
 
 
+@pytest.mark.parametrize("B,T", [(1, 1100), (2, 2053)])
+def test_long_rows_with_state(cuda_lib, B, T):
+    """Several fixed-length rows of many chunks, a ragged last chunk and a carried h0."""
+    w = Workload("case", (T,) * B, 1, 2, 128, 128, 64, "bf16", h0_std=0.1, seed=20 + B)
+    x = make_inputs(w, device="cuda")
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=range(2), seqs=list(range(B)), dtype="bf16")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_chunk_128_is_the_same_function(cuda_lib, dtype):
     """chunk = 128 runs as two 64-token chunks: bit-identical to chunk = 64, and the
