@@ -135,7 +135,8 @@ class ClockSampler:
 
 
 def run_decode(lap, w, dev, steps=200):
-    """µs per gdn_recurrent_step on this workload's state shape, plain and as a CUDA graph."""
+    """µs per decode step on this workload's state shape, plain and as a CUDA graph."""
+    stepfn = lap.ssd_recurrent_step if w.op == "ssd" else lap.gdn_recurrent_step
     N, Hv = w.n_seqs, w.Hv
     h = torch.randn((N, Hv, w.dk, w.dv), device=dev) * 0.1
     d = make_decode_inputs(w, 0, device=dev)
@@ -143,7 +144,7 @@ def run_decode(lap, w, dev, steps=200):
     stream = torch.cuda.current_stream(dev)
 
     def one():
-        lap.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], h, o)
+        stepfn(d["q"], d["k"], d["v"], d["g"], d["beta"], h, o)
 
     for _ in range(10):
         one()
@@ -185,19 +186,20 @@ def run_decode(lap, w, dev, steps=200):
 
 def oracle_tokens_per_s(w, x_cpu, budget_s):
     """fp64 oracle (one core) on the first tokens of every head; returns (tok/s, sample)."""
-    from oracle import gdn_recurrent
+    from oracle import gdn_recurrent, ssd_recurrent
+    fwd = ssd_recurrent if w.op == "ssd" else gdn_recurrent
     H = w.Hv
     # calibrate: a few tokens of every head
     probe = 16
     t = time.perf_counter()
     sl = {k_: v_[:, :probe] for k_, v_ in x_cpu.items() if k_ in ("q", "k", "v", "g", "beta")}
-    gdn_recurrent(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, x_cpu["h0"][:1] if x_cpu["h0"] is not None else None)
+    fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, x_cpu["h0"][:1] if x_cpu["h0"] is not None else None)
     per_tok = (time.perf_counter() - t) / probe
     n_tok = int(max(probe, min(w.seqlens[0], budget_s / per_tok)))
     sl = {k_: v_[:, :n_tok] for k_, v_ in x_cpu.items() if k_ in ("q", "k", "v", "g", "beta")}
     h0 = x_cpu["h0"][:1] if x_cpu["h0"] is not None else None
     t = time.perf_counter()
-    gdn_recurrent(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, h0)
+    fwd(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], w.scale, h0)
     dt = time.perf_counter() - t
     return n_tok / dt, f"first {n_tok} tokens of sequence 0, all {H} v heads, fp64 numpy, 1 thread", dt
 
@@ -246,9 +248,11 @@ def bench_cuda(args, w, rank, world, local_rank):
     o = torch.empty_like(x["v"])
     hT = torch.empty((w.n_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
 
+    fwd = lap.ssd_chunk_fwd if w.op == "ssd" else lap.gdn_chunk_fwd
+
     def step():
-        lap.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT,
-                          chunk=w.chunk, cu_seqlens=x["cu_seqlens"], stream=stream)
+        fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
+            scale=w.scale, cu_seqlens=x["cu_seqlens"], stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -282,7 +286,7 @@ def bench_cuda(args, w, rank, world, local_rank):
             for k_ in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")}
     out = {}
     for _ in range(max(1, args.warmup)):
-        lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out)
+        lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out, op=w.op)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 50))
     if world > 1:
@@ -290,7 +294,8 @@ def bench_cuda(args, w, rank, world, local_rank):
     t0 = time.perf_counter()
     bi = bo = 0
     for _ in range(e2e_steps):
-        o_h, hT_h, bi, bo = lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out)
+        o_h, hT_h, bi, bo = lap.gdn_chunk_fwd_host(host, chunk=w.chunk, device=dev, out=out,
+                                                   op=w.op)
         torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
     e2e_ms, e2e_tok = reduce_timing(e2e_s * 1e3, float(w.T_total * e2e_steps))

@@ -163,6 +163,45 @@ gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v
                                   gdn_stream_t stream);
 
 /*
+ * Mamba-2 SSD scan - the same chunked scan without the delta rule's erase term
+ * ("Exp 2026-07-13 — Linear-Attention Scans on the NPU", §1 and §3: the SSM
+ * scan's four matrix stages per chunk - the C B^T gram, the intra-chunk output,
+ * the chunk state and the inter-chunk output).  Per (sequence, v head), tokens
+ * in order, with C -> q, B -> k, x -> v, the per-token log-decay dt A -> g and
+ * the input step dt -> beta:
+ *
+ *   S_t = exp(g_t) S_{t-1} + beta_t v_t k_t^T,      o_t = S_t (scale q_t)
+ *
+ * (the gated delta rule above with (I - beta_t k_t k_t^T) replaced by I; the
+ * state is h = S^T, [dk = d_state][dv = head_dim]).  Arguments, layouts, sizes,
+ * grouping of q/k heads (B/C groups), workspace (gdn_chunk_fwd_workspace_size)
+ * and errors are those of the gdn_* counterpart; beta may exceed 1 here.  The
+ * same kernels run with the KKT gram and the W term switched off (Tm = I,
+ * W = 0, U = diag(beta) V).
+ */
+gdn_status ssd_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream);
+gdn_status ssd_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream);
+gdn_status ssd_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
+                             const float* beta, const float* h0, float* o, float* hT, int B,
+                             int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                             const int32_t* cu_seqlens, gdn_stream_t stream);
+/* one decode token of the SSD recurrence: h <- exp(g) h + beta k v^T; o = h^T (scale q) */
+gdn_status ssd_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream);
+gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v,
+                                  const float* g, const float* beta, float* h, float* o, int N,
+                                  int Hqk, int Hv, int dk, int dv, float scale,
+                                  gdn_stream_t stream);
+
+/*
  * gdn_device_status - waits for `stream`, then reads and clears the device
  * error word that bounded device-side waits set when they give up.  Returns
  * GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the stream itself failed.

@@ -33,6 +33,11 @@ SIGNATURES = {
     "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
     "gdn_recurrent_step": (_I, _STEP_ARGS),
     "gdn_recurrent_step_f32": (_I, _STEP_ARGS),
+    "ssd_chunk_fwd": (_I, _FWD_ARGS),
+    "ssd_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "ssd_chunk_fwd_f32": (_I, _FWD_ARGS),
+    "ssd_recurrent_step": (_I, _STEP_ARGS),
+    "ssd_recurrent_step_f32": (_I, _STEP_ARGS),
     "gdn_device_status": (_I, [_P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
     "gdn_last_error": (ctypes.c_char_p, []),
@@ -108,7 +113,7 @@ def gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) 
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
                   stream=None, workspace=None):
-    """Chunked-prefill forward; returns (o, hT).
+    """Chunked-prefill forward of the gated delta rule; returns (o, hT).
 
     q, k [B, T, Hqk, dk]; v [B, T, Hv, dv] (bf16 or fp32, all the same);
     g, beta [B, T, Hv] fp32; h0 [N, Hv, dk, dv] fp32 or None.  With
@@ -116,8 +121,26 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
     o and hT may be passed preallocated; hT may be h0 (in place).  The bf16
     path runs gdn_chunk_fwd_ex with ``workspace`` (a uint8 device tensor of at
     least gdn_chunk_fwd_workspace_size bytes) or a fresh one from torch's
-    caching allocator.
+    caching allocator.  ``scale`` defaults to dk^-0.5.
     """
+    return _chunk_fwd("gdn", q, k, v, g, beta, h0, o, hT, chunk,
+                      k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
+                      output_final_state, stream, workspace)
+
+
+def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
+                  scale: float = 1.0, cu_seqlens=None, output_final_state=True, stream=None,
+                  workspace=None):
+    """Chunked Mamba-2 SSD scan (the same recurrence without the erase term):
+    S_t = exp(g_t) S_{t-1} + beta_t v_t k_t^T, o_t = S_t (scale q_t), with
+    C -> q, B -> k, x -> v, dt A -> g, dt -> beta.  Arguments as gdn_chunk_fwd;
+    ``scale`` defaults to 1.  Returns (o, hT)."""
+    return _chunk_fwd("ssd", q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens,
+                      output_final_state, stream, workspace)
+
+
+def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output_final_state,
+               stream, workspace):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -148,28 +171,36 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
         hT = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
     if hT is not None:
         _need(hT, "hT", torch.float32, dev, (N, Hv, dk, dv))
-    if scale is None:
-        scale = dk ** -0.5
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
             N, T, Hqk, Hv, dk, dv, chunk, float(scale), _ptr(cu_seqlens))
     if dt == torch.float32:
-        _check(lib.gdn_chunk_fwd_f32(*args, _stream_handle(stream, dev)))
+        _check(getattr(lib, f"{op}_chunk_fwd_f32")(*args, _stream_handle(stream, dev)))
         return o, hT
     need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk, cu_seqlens is not None)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
-    _check(lib.gdn_chunk_fwd_ex(*args, _ptr(workspace), workspace.numel(),
-                                _stream_handle(stream, dev)))
+    _check(getattr(lib, f"{op}_chunk_fwd_ex")(*args, _ptr(workspace), workspace.numel(),
+                                              _stream_handle(stream, dev)))
     return o, hT
 
 
 def gdn_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = None,
                        stream=None):
-    """One decode token; updates h in place and returns o.
+    """One decode token of the gated delta rule; updates h in place and returns o.
 
     q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv] fp32; h [N, Hv, dk, dv] fp32.
     """
+    return _step("gdn", q, k, v, g, beta, h, o, k.shape[-1] ** -0.5 if scale is None else scale,
+                 stream)
+
+
+def ssd_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: float = 1.0, stream=None):
+    """One decode token of the Mamba-2 SSD recurrence; updates h in place, returns o."""
+    return _step("ssd", q, k, v, g, beta, h, o, scale, stream)
+
+
+def _step(op, q, k, v, g, beta, h, o, scale, stream):
     lib = load_library()
     dev = q.device
     dt = q.dtype
@@ -184,9 +215,7 @@ def gdn_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = 
     if o is None:
         o = torch.empty((N, Hv, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev, (N, Hv, dv))
-    if scale is None:
-        scale = dk ** -0.5
-    fn = lib.gdn_recurrent_step if dt == torch.bfloat16 else lib.gdn_recurrent_step_f32
+    fn = getattr(lib, f"{op}_recurrent_step" + ("" if dt == torch.bfloat16 else "_f32"))
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h), _ptr(o), N, Hqk, Hv,
               dk, dv, float(scale), _stream_handle(stream, dev)))
     return o
@@ -198,8 +227,10 @@ def gdn_device_status(stream=None):
     _check(load_library().gdn_device_status(_stream_handle(stream, dev)))
 
 
-def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None):
-    """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out.
+def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None,
+                       op: str = "gdn"):
+    """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out
+    (``op`` "ssd" runs ssd_chunk_fwd instead).
 
     ``inputs`` holds pinned CPU tensors q, k, v, g, beta and optionally h0 and
     cu_seqlens.  ``out`` may hold preallocated pinned (o, hT) host tensors and
@@ -220,10 +251,10 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         buf.copy_(t, non_blocking=True)
         d[name] = buf
         nbytes_in += t.numel() * t.element_size()
-    o_dev, hT_dev = gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
-                                  bufs.get("o"), bufs.get("hT"), chunk=chunk,
-                                  cu_seqlens=d["cu_seqlens"], stream=stream,
-                                  workspace=bufs.get("workspace"))
+    fwd = ssd_chunk_fwd if op == "ssd" else gdn_chunk_fwd
+    o_dev, hT_dev = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], bufs.get("o"),
+                        bufs.get("hT"), chunk=chunk, cu_seqlens=d["cu_seqlens"], stream=stream,
+                        workspace=bufs.get("workspace"))
     bufs["o"], bufs["hT"] = o_dev, hT_dev
     if out is not None and "o_host" in out:
         o_h, hT_h = out["o_host"], out["hT_host"]

@@ -89,6 +89,7 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   p->err = nullptr;
   p->N = B; p->T = T; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->chunk = chunk;
   p->scale = scale;
+  p->delta_rule = 1;
   return GDN_OK;
 }
 
@@ -121,6 +122,7 @@ gdn_status check_step(const void* q, const void* k, const void* v, const float* 
     return fail(GDN_ERR_INVALID_ARG, "misaligned pointer (16 bytes for tensors, 4 for g, beta)");
   p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->h = h; p->o = o;
   p->N = N; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->scale = scale;
+  p->delta_rule = 1;
   return GDN_OK;
 }
 
@@ -161,6 +163,25 @@ gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cuda
   return GDN_OK;
 }
 
+// bf16 forward on a workspace taken from the stream-ordered pool and given back after.
+gdn_status fwd_bf16_pooled(const gdn::FwdParams& p, cudaStream_t st) {
+  if (p.N == 0 || (!p.cu_seqlens && p.T == 0)) return run_fwd_bf16(p, nullptr, 0, st);
+  const size_t bytes = gdn::ws_bytes(gdn::ws_layout(p, nullptr), p.Hv);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "allocating the workspace");
+  gdn_status s = run_fwd_bf16(p, ws, bytes, st);
+  e = cudaFreeAsync(ws, st);
+  if (s == GDN_OK && e != cudaSuccess) return cuda_fail(e, "freeing the workspace");
+  return s;
+}
+
+gdn_status run_step(const gdn::StepParams& p, bool f32, cudaStream_t st) {
+  if (p.N == 0) return GDN_OK;
+  cudaError_t e = f32 ? gdn::launch_step_f32(p, st) : gdn::launch_step_bf16(p, st);
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,16 +218,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (p.N == 0 || (!cu_seqlens && T == 0)) return run_fwd_bf16(p, nullptr, 0, st);
-  const size_t bytes = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
-  void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, bytes, st);
-  if (e != cudaSuccess) return cuda_fail(e, "allocating the workspace");
-  s = run_fwd_bf16(p, ws, bytes, st);
-  e = cudaFreeAsync(ws, st);
-  if (s == GDN_OK && e != cudaSuccess) return cuda_fail(e, "freeing the workspace");
-  return s;
+  return fwd_bf16_pooled(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
@@ -226,9 +238,7 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
   gdn::StepParams p;
   gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
   if (s != GDN_OK) return s;
-  if (N == 0) return GDN_OK;
-  cudaError_t e = gdn::launch_step_bf16(p, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
+  return run_step(p, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v,
@@ -238,9 +248,66 @@ gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v
   gdn::StepParams p;
   gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
   if (s != GDN_OK) return s;
-  if (N == 0) return GDN_OK;
-  cudaError_t e = gdn::launch_step_f32(p, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
+  return run_step(p, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- the same kernels without the erase term: Mamba-2 SSD ---------------------
+gdn_status ssd_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  p.delta_rule = 0;
+  return fwd_bf16_pooled(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status ssd_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  p.delta_rule = 0;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status ssd_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
+                             const float* beta, const float* h0, float* o, float* hT, int B,
+                             int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                             const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 4, &p);
+  if (s != GDN_OK) return s;
+  p.delta_rule = 0;
+  return run_fwd_f32(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status ssd_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  p.delta_rule = 0;
+  return run_step(p, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v,
+                                  const float* g, const float* beta, float* h, float* o, int N,
+                                  int Hqk, int Hv, int dk, int dv, float scale,
+                                  gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  p.delta_rule = 0;
+  return run_step(p, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_device_status(gdn_stream_t stream) {

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_f32_kernel(const FwdParam
           const int r = ti + 16 * a, cc = tj + 16 * b;
           const bool low = r >= cc && r < L;
           const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
-          s.A[r * LDA + cc] = (low && r > cc) ? s.beta[r] * m * sk[a][b] : 0.f;
+          s.A[r * LDA + cc] = (low && r > cc && p.delta_rule) ? s.beta[r] * m * sk[a][b] : 0.f;
           s.P[r * LDA + cc] = low ? p.scale * m * sq[a][b] : 0.f;
         }
     }
@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_f32_kernel(const FwdParam
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int r = ti + 16 * a;
-        const float br = s.beta[r], bgr = s.beta[r] * s.gam[r], sg = p.scale * s.gam[r];
+        const float br = s.beta[r], sg = p.scale * s.gam[r];
+        const float bgr = p.delta_rule ? s.beta[r] * s.gam[r] : 0.f;  // no K h term without the erase
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const int cc = tj + 16 * b;

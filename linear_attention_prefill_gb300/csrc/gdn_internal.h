@@ -24,6 +24,7 @@ struct FwdParams {
   int Hqk, Hv, dk, dv, chunk;
   float scale;
   unsigned* err;      // device error word: bounded waits record a timeout here
+  int delta_rule;     // 1: gated delta rule (GDN); 0: no erase term (Mamba-2 SSD scan)
 };
 
 // One decode step.
@@ -37,6 +38,7 @@ struct StepParams {
   void* o;            // [N, Hv, dv]
   int N, Hqk, Hv, dk, dv;
   float scale;
+  int delta_rule;     // 1: gated delta rule; 0: no erase term (Mamba-2 SSD)
 };
 
 // Workspace of the bf16 forward: one record per (chunk slot, v head), written

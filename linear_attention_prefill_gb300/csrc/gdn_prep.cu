@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     s_e[r1] = expf(Glast - G1);
     s_beta[r0] = b0;
     s_beta[r1] = b1;
-    s_bg[r0] = b0 * gam0;
-    s_bg[r1] = b1 * gam1;
+    s_bg[r0] = p.delta_rule ? b0 * gam0 : 0.f;  // W's column factor: 0 without the erase
+    s_bg[r1] = p.delta_rule ? b1 * gam1 : 0.f;
     float* gv = ws.gv(slot, hv, p.Hv);  // gamma_last, then gamma of every row
     if (lane == 31) gv[0] = expf(Glast);
     *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     float x[32];
     tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + c0, x);
     const float Gr = s_G[r], rowf = isP ? p.scale : s_beta[r];
-    const int lim = isP ? r : r - 1;  // last column kept
+    // last column kept; without the erase term (SSD) A is zero, so Tm = I and U = diag(beta) V
+    const int lim = isP ? r : (p.delta_rule ? r - 1 : -1);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int cc = c0 + j;

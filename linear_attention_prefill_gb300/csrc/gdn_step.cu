@@ -6,6 +6,8 @@
 //
 // Per token, with h = S^T of shape [dk, dv]:
 //   h <- exp(g) h;  u = beta (v - h^T k);  h <- h + k u^T;  o = h^T (scale q)
+// and, without the erase term (the Mamba-2 SSD recurrence of "Exp 2026-07-13 —
+// Linear-Attention Scans on the NPU", §1 and §3), u = beta v.
 // The state is read once and written once, so the step is bound by HBM
 // bandwidth: each CTA streams a [dk, 32] column tile of h with 128-byte
 // coalesced rows, keeps it in registers between the two column reductions.
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
   float kh = 0.f;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) kh += red1[w][lane];
-  const float u = b * (vcol - kh);
+  const float u = b * (p.delta_rule ? vcol - kh : vcol);  // no erase term: u = beta v
   part = 0.f;
 #pragma unroll
   for (int i = 0; i < R; ++i) {

@@ -66,8 +66,15 @@ def macs_per_token_head(chunk, dk, dv):
     return kkt + qkt + wu + solve + state + pv
 
 
-def flops(T_total, Hv, chunk, dk, dv):
-    return 2.0 * T_total * Hv * macs_per_token_head(chunk, dk, dv)
+def ssd_macs_per_token_head(chunk, dk, dv):
+    """The SSD scan's four stages: C B^T gram, intra-chunk output, Q h, state update."""
+    C = chunk
+    return (C + 1) / 2 * dk + (C + 1) / 2 * dv + 2 * dk * dv
+
+
+def flops(T_total, Hv, chunk, dk, dv, op="gdn"):
+    per = macs_per_token_head if op == "gdn" else ssd_macs_per_token_head
+    return 2.0 * T_total * Hv * per(chunk, dk, dv)
 
 
 def decode_bytes(n_seqs, Hqk, Hv, dk, dv, elem_bytes):
@@ -85,7 +92,7 @@ def workload_model(w, peaks):
     eb = 4 if w.dtype == "f32" else 2
     b = io_bytes(w.T_total, w.n_seqs, w.Hqk, w.Hv, w.dk, w.dv, eb,
                  h0_read=w.h0_std is not None, hT_written=True)
-    f = flops(w.T_total, w.Hv, w.chunk, w.dk, w.dv)
+    f = flops(w.T_total, w.Hv, w.chunk, w.dk, w.dv, getattr(w, "op", "gdn"))
     t_hbm = b / (peaks["hbm_gbs"] * 1e9)
     if w.dtype == "f32":
         tc = fp32_alu_tflops(peaks.get("sm_max_mhz", 2070.0)) * 1e12

@@ -45,6 +45,7 @@ class Workload:
     g_mu: float = 0.0       # g = -softplus(N(g_mu, 1)) * g_scale
     g_scale: float = 1.0
     h0_std: Optional[float] = None   # None: no initial state (zeros)
+    op: str = "gdn"                  # "gdn" (gated delta rule) or "ssd" (Mamba-2 scan)
     varlen: bool = False    # True: one packed [1, T_total, ...] batch with cu_seqlens
     seed: int = 0
     decode_steps: int = 0   # one-token steps that continue from the final state
@@ -59,7 +60,7 @@ class Workload:
 
     @property
     def scale(self) -> float:
-        return float(self.dk) ** -0.5
+        return float(self.dk) ** -0.5 if self.op == "gdn" else 1.0
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -92,6 +93,11 @@ WORKLOADS["long_64k_strong_c128"] = WORKLOADS["long_64k_strong"].replace(
     name="long_64k_strong_c128", chunk=128)
 WORKLOADS["long_64k_weak_c128"] = WORKLOADS["long_64k_weak"].replace(
     name="long_64k_weak_c128", chunk=128)
+
+# Mamba-2 SSD scan of a 2.7B-class model ("Exp 2026-07-13 — Linear-Attention Scans on the
+# NPU", §3: head_dim 64, d_state 128, chunks of 64; 80 heads sharing one B/C group), 4K prompt.
+WORKLOADS["ssd_80h_4k"] = Workload("ssd_80h_4k", (4096,), 1, 80, 128, 64, 64, "bf16", seed=6,
+                                   op="ssd")
 
 # The workload the headline throughput is quoted on.
 HEADLINE = "layer_16h_4k"
@@ -136,8 +142,14 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
     q = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
     k = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
     v = randn(B, T, w.Hv, w.dv).to(dt)
-    beta = torch.sigmoid(randn(B, T, w.Hv))
-    g = -torch.nn.functional.softplus(randn(B, T, w.Hv) + w.g_mu) * w.g_scale
+    if w.op == "ssd":
+        # dt = softplus(N(0, 1)) is the input step (beta); g = dt * A with A = -exp(N(0, 0.3))
+        # per head
+        beta = torch.nn.functional.softplus(randn(B, T, w.Hv))
+        g = -beta * torch.exp(0.3 * randn(w.Hv))
+    else:
+        beta = torch.sigmoid(randn(B, T, w.Hv))
+        g = -torch.nn.functional.softplus(randn(B, T, w.Hv) + w.g_mu) * w.g_scale
     h0 = None
     if w.h0_std is not None:
         h0 = randn(N, w.Hv, w.dk, w.dv) * w.h0_std
@@ -161,6 +173,10 @@ def make_decode_inputs(w: Workload, step: int, device="cpu") -> dict:
     q = _unit_rows(randn(N, w.Hqk, w.dk)).to(dt)
     k = _unit_rows(randn(N, w.Hqk, w.dk)).to(dt)
     v = randn(N, w.Hv, w.dv).to(dt)
-    beta = torch.sigmoid(randn(N, w.Hv))
-    g = -torch.nn.functional.softplus(randn(N, w.Hv) + w.g_mu) * w.g_scale
+    if w.op == "ssd":
+        beta = torch.nn.functional.softplus(randn(N, w.Hv))
+        g = -beta * torch.exp(0.3 * randn(w.Hv))
+    else:
+        beta = torch.sigmoid(randn(N, w.Hv))
+        g = -torch.nn.functional.softplus(randn(N, w.Hv) + w.g_mu) * w.g_scale
     return dict(q=q, k=k, v=v, g=g.contiguous(), beta=beta.contiguous(), N=N, scale=w.scale)

@@ -1,10 +1,14 @@
-"""fp64 CPU oracle for the Gated DeltaNet chunked-prefill forward (test infrastructure only).
+"""fp64 CPU oracle for the Gated DeltaNet chunked-prefill forward and the Mamba-2
+SSD scan (test infrastructure only).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU baseline and
 reference arm may import this package.  The product path never does.
 """
 from .gdn_oracle import (gdn_dense, gdn_recurrent, gdn_chunked, gdn_step, chains, qk_head,
                          forward_substitution_inverse, recurrent_chain, chunked_chain)
+from .ssd_oracle import (ssd_recurrent, ssd_unrolled, ssd_chunked, ssd_step,
+                         ssd_recurrent_chain)
 
 __all__ = ["gdn_dense", "gdn_recurrent", "gdn_chunked", "gdn_step", "chains", "qk_head",
-           "forward_substitution_inverse", "recurrent_chain", "chunked_chain"]
+           "forward_substitution_inverse", "recurrent_chain", "chunked_chain",
+           "ssd_recurrent", "ssd_unrolled", "ssd_chunked", "ssd_step", "ssd_recurrent_chain"]

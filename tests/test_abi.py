@@ -20,14 +20,16 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gdn|ssd)_\w+)\s*\(", text,
+                                 flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_recurrent_step",
                  "gdn_recurrent_step_f32", "gdn_status_string", "gdn_last_error",
-                 "gdn_device_status", "gdn_abi_version"):
+                 "gdn_device_status", "gdn_abi_version", "ssd_chunk_fwd", "ssd_chunk_fwd_ex",
+                 "ssd_chunk_fwd_f32", "ssd_recurrent_step", "ssd_recurrent_step_f32"):
         assert want in names
 
 
@@ -51,11 +53,12 @@ A = 0x10000  # an aligned fake address: never dereferenced, validation fails fir
 
 
 def fwd(lib, q=A, k=A, v=A, g=A, beta=A, h0=None, o=A, hT=None, B=1, T=128, Hqk=1, Hv=2,
-        dk=128, dv=128, chunk=64, scale=0.088, cu=None, f32=False):
-    fn = lib.gdn_chunk_fwd_f32 if f32 else lib.gdn_chunk_fwd
+        dk=128, dv=128, chunk=64, scale=0.088, cu=None, f32=False, op="gdn"):
+    fn = getattr(lib, f"{op}_chunk_fwd" + ("_f32" if f32 else ""))
     return fn(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale, cu, None)
 
 
+@pytest.mark.parametrize("op", ["gdn", "ssd"])
 @pytest.mark.parametrize("f32", [False, True])
 @pytest.mark.parametrize("case,status", [
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(g=None), 1),
@@ -70,25 +73,26 @@ def fwd(lib, q=A, k=A, v=A, g=A, beta=A, h0=None, o=A, hT=None, B=1, T=128, Hqk=
     (dict(T=1 << 30, B=4096), 1),
     (dict(cu=A, B=0), 1),
 ])
-def test_forward_rejects_bad_arguments(lib, case, status, f32):
-    assert fwd(lib, f32=f32, **case) == status
+def test_forward_rejects_bad_arguments(lib, case, status, f32, op):
+    assert fwd(lib, f32=f32, op=op, **case) == status
     assert lib.gdn_last_error() != b""
 
 
 def step(lib, q=A, k=A, v=A, g=A, beta=A, h=A, o=A, N=2, Hqk=1, Hv=2, dk=128, dv=128,
-         scale=0.088, f32=False):
-    fn = lib.gdn_recurrent_step_f32 if f32 else lib.gdn_recurrent_step
+         scale=0.088, f32=False, op="gdn"):
+    fn = getattr(lib, f"{op}_recurrent_step" + ("_f32" if f32 else ""))
     return fn(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, None)
 
 
+@pytest.mark.parametrize("op", ["gdn", "ssd"])
 @pytest.mark.parametrize("f32", [False, True])
 @pytest.mark.parametrize("case,status", [
     (dict(q=None), 1), (dict(h=None), 1), (dict(o=None), 1), (dict(N=-1), 1),
     (dict(Hqk=2, Hv=3), 1), (dict(dk=80), 2), (dict(dv=256), 2), (dict(h=A + 4), 1),
     (dict(scale=float("nan")), 1),
 ])
-def test_step_rejects_bad_arguments(lib, case, status, f32):
-    assert step(lib, f32=f32, **case) == status
+def test_step_rejects_bad_arguments(lib, case, status, f32, op):
+    assert step(lib, f32=f32, op=op, **case) == status
 
 
 def test_no_op_calls_return_ok_without_a_device(lib):
