@@ -148,8 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
         uint64_t* bar = &full[c % kStages];
         const long long slot = slot0 + c;
-        mbar_expect_tx(bar, Lo::kTx);
-        bulk_g2s(st + Lo::kWt, ws.W(slot, hv, p.Hv), kC * DK * 2, bar);
+        // without the erase term (SSD) W is zero: it is neither formed nor loaded
+        mbar_expect_tx(bar, p.delta_rule ? Lo::kTx : Lo::kTx - kC * DK * 2);
+        if (p.delta_rule) bulk_g2s(st + Lo::kWt, ws.W(slot, hv, p.Hv), kC * DK * 2, bar);
         bulk_g2s(st + Lo::kKt, ws.Kt(slot, hv, p.Hv), kC * DK * 2, bar);
         bulk_g2s(st + Lo::kP, ws.P(slot, hv, p.Hv), kC * kC * 2, bar);
         bulk_g2s(st + Lo::kUt, ws.U(slot, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
@@ -260,8 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(&full[c % kStages], (c / kStages) & 1, p.err)) *s_abort = 1;
     GDN_PHASE(17);  // wait for staging
     uint32_t wa[DK / 16][4];  // W rows of this warp, all k steps
+    if (p.delta_rule) {
 #pragma unroll
-    for (int ks = 0; ks < DK / 16; ++ks) load_a_trans_sw<kC>(wa[ks], Wt, 16 * warp, 16 * ks, lane);
+      for (int ks = 0; ks < DK / 16; ++ks) load_a_trans_sw<kC>(wa[ks], Wt, 16 * warp, 16 * ks, lane);
+    }
     uint32_t ka[kC / 16][MTW][4];  // Kt^T rows of this warp, all k steps
 #pragma unroll
     for (int ks = 0; ks < kC / 16; ++ks)
@@ -279,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int x = 0; x < 4; ++x) wh[hh][j][x] = 0.f;
+      if (p.delta_rule) {  // SSD: V_new = U
 #pragma unroll
       for (int ks = 0; ks < DK / 32; ++ks) {
 #pragma unroll
@@ -292,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16(wh[hh][j + 1], wa[kk / 16], bb[2], bb[3]);
           }
         }
+      }
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {

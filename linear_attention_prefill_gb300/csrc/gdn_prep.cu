@@ -289,8 +289,19 @@ __global__ void __launch_bounds__(kThreads, 4)
   // Diagonal 16x16 blocks in fp32 (warp b, lane l = column l of block b), by
   // right-looking substitution: once x_m is final it updates every x_i, i > m,
   // so the dependent chain is 15 FMAs deep.  Warps 4-7 zero the strictly upper
-  // blocks meanwhile.
-  if (!*s_abort) {
+  // blocks meanwhile.  Without the erase term (SSD) A = 0: Tm = I, so only
+  // Tu = diag(beta) is needed (W is zero and never formed).
+  const bool delta = p.delta_rule != 0;  // uniform over the grid
+  if (!*s_abort && !delta) {
+    for (int e = tid; e < kC * 8; e += kThreads) {  // 16-byte chunks of Tu, diagonal inside
+      const int rr = e >> 3, ch = e & 7;
+      __align__(16) __half z[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) z[i] = __float2half_rn(rr == 8 * ch + i ? s_beta[rr] : 0.f);
+      *reinterpret_cast<uint4*>(&Tu[sw128(rr, 8 * ch)]) = *reinterpret_cast<const uint4*>(z);
+    }
+  }
+  if (!*s_abort && delta) {
     if (warp < 4) {
       if (lane < 16) {
         const int b = warp, l = lane;
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   __syncthreads();
   GDN_STAMP(34, 0);  // diagonal blocks done
   GDN_STAMP(40, 128);
-  if (!*s_abort) {
+  if (!*s_abort && delta) {
     if (warp < 2) {
       // level 1: T10 = -(T11 A10) T00 (warp 0), T32 = -(T33 A32) T22 (warp 1)
       {
@@ -401,20 +412,22 @@ __global__ void __launch_bounds__(kThreads, 4)
       for (int vb = 0; vb < DV / 64; ++vb)
         tma_load_2d(sm + Lo::kV + vb * Lo::kVStride, &tmv, hv * DV + vb * 64, t0, bar_v);
     }
-    tc_fence_after();
-    constexpr uint32_t idw = idesc_f16(DK, 64, true, true, false);
+    if (delta) {
+      tc_fence_after();
+      constexpr uint32_t idw = idesc_f16(DK, 64, true, true, false);
 #pragma unroll
-    for (int s = 0; s < kC / 16; ++s)
-      tc_mma(tmem + 64, sw128_desc(sbase + s * 2048, 16384, 1024),
-             sw128_desc(sbase + Lo::kTw + s * 32, 16, 1024), idw, s > 0);
-    tc_commit(bar_w);
+      for (int s = 0; s < kC / 16; ++s)
+        tc_mma(tmem + 64, sw128_desc(sbase + s * 2048, 16384, 1024),
+               sw128_desc(sbase + Lo::kTw + s * 32, 16, 1024), idw, s > 0);
+      tc_commit(bar_w);
+    }
   }
   // tensor-memory lane -> d: lane d for M = 128; rows 16q + i sit in lanes 32q + i for M = 64
   const int q4 = warp & 3, h = warp >> 2;
   const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
-  if (tid == 0 && !*s_abort && !mbar_wait(bar_w, 0, p.err)) *s_abort = 1;
-  __syncthreads();
-  if (!*s_abort) {
+  if (delta && tid == 0 && !*s_abort && !mbar_wait(bar_w, 0, p.err)) *s_abort = 1;
+  if (delta) __syncthreads();
+  if (!*s_abort && delta) {
     mbar_wait(bar_w, 0, p.err);
     tc_fence_after();
     float x[32];
