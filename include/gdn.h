@@ -208,6 +208,17 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
  */
 gdn_status gdn_device_status(gdn_stream_t stream);
 
+/*
+ * gdn_selftest_expired_wait - diagnostic for the timeout path: enqueues one
+ * warp that waits on a device barrier nothing ever completes, giving up after
+ * `limit_cycles` SM clock cycles (0 .. 2^31; the kernels' own waits use
+ * 2^31, about a second).  The expired wait records the timeout in the device
+ * error word, so the next gdn_device_status returns GDN_ERR_TIMEOUT (and
+ * clears it); the kernel returns normally and leaves the context usable.
+ * Returns GDN_OK once enqueued.
+ */
+gdn_status gdn_selftest_expired_wait(long long limit_cycles, gdn_stream_t stream);
+
 /* Static description of a status code. */
 const char* gdn_status_string(gdn_status s);
 

@@ -6,9 +6,10 @@ workloads and the algorithmic byte/FLOP model.  The same kernels also run the
 Mamba-2 SSD scan (the recurrence without the delta rule's erase term).
 """
 from .binding import (GdnError, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_workspace_size,
-                      gdn_device_status, gdn_recurrent_step, load_library, ssd_chunk_fwd,
-                      ssd_recurrent_step, status_string)
+                      gdn_device_status, gdn_recurrent_step, gdn_selftest_expired_wait,
+                      load_library, ssd_chunk_fwd, ssd_recurrent_step, status_string)
 
 __all__ = ["GdnError", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_workspace_size",
-           "gdn_device_status", "gdn_recurrent_step", "load_library", "ssd_chunk_fwd",
+           "gdn_device_status", "gdn_recurrent_step", "gdn_selftest_expired_wait", "load_library",
+           "ssd_chunk_fwd",
            "ssd_recurrent_step", "status_string"]

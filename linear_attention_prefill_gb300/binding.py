@@ -39,6 +39,7 @@ SIGNATURES = {
     "ssd_recurrent_step": (_I, _STEP_ARGS),
     "ssd_recurrent_step_f32": (_I, _STEP_ARGS),
     "gdn_device_status": (_I, [_P]),
+    "gdn_selftest_expired_wait": (_I, [ctypes.c_longlong, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
     "gdn_last_error": (ctypes.c_char_p, []),
     "gdn_abi_version": (_I, []),
@@ -219,6 +220,12 @@ def _step(op, q, k, v, g, beta, h, o, scale, stream):
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h), _ptr(o), N, Hqk, Hv,
               dk, dv, float(scale), _stream_handle(stream, dev)))
     return o
+
+
+def gdn_selftest_expired_wait(limit_cycles: int = 1 << 20, stream=None):
+    """Enqueue the timeout-path diagnostic (a bounded wait that is bound to expire)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(load_library().gdn_selftest_expired_wait(int(limit_cycles), _stream_handle(stream, dev)))
 
 
 def gdn_device_status(stream=None):

@@ -32,6 +32,19 @@ cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
   return err;
 }
 
+// Diagnostic: one warp waits on an mbarrier that nothing ever completes, with a
+// limit of `limit` cycles; the expired wait records kErrWaitTimeout in the error
+// word and the kernel returns normally (no trap, no fault, nothing left pending).
+__global__ void selftest_expired_wait_kernel(unsigned* err, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, err, limit);
+}
+
 }  // namespace gdn
 
 namespace {
@@ -308,6 +321,18 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
   if (s != GDN_OK) return s;
   p.delta_rule = 0;
   return run_step(p, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_selftest_expired_wait(long long limit_cycles, gdn_stream_t stream) {
+  if (limit_cycles < 0 || limit_cycles > (1ll << 31))
+    return fail(GDN_ERR_INVALID_ARG, "limit_cycles=%lld must be in [0, 2^31]", limit_cycles);
+  unsigned* err = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), gdn::g_device_error);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the device error word");
+  gdn::selftest_expired_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      err, limit_cycles);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the expired-wait self-test");
 }
 
 gdn_status gdn_device_status(gdn_stream_t stream) {

@@ -86,9 +86,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
                "r"(bytes)
                : "memory");
 }
-// Wait for phase `parity` of `bar` to complete, giving up after ~2^31 cycles
-// (about a second): returns false then, and records kErrWaitTimeout in *err.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned* err) {
+// Wait for phase `parity` of `bar` to complete, giving up after `limit` cycles:
+// returns false then, and records kErrWaitTimeout in *err.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, unsigned parity, unsigned* err,
+                                                long long limit) {
   const long long t0 = clock64();
   unsigned done = 0;
   while (true) {
@@ -99,11 +100,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     if (done) return true;
-    if (clock64() - t0 > (1ll << 31)) {
-      if (err) atomicExch(err, 1u);
+    if (clock64() - t0 > limit) {
+      if (err) atomicExch(err, kErrWaitTimeout);
       return false;
     }
   }
+}
+// The kernels' wait: gives up after ~2^31 cycles (about a second).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned* err) {
+  return mbar_wait_limit(bar, parity, err, 1ll << 31);
 }
 // global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned;
 // completion is counted on `bar` (its transaction count must expect the bytes).
