@@ -163,6 +163,39 @@ gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v
                                   gdn_stream_t stream);
 
 /*
+ * gdn_chunk_fwd_prologue(_ex) - gdn_chunk_fwd with the projection-side
+ * elementwise steps fused into the first kernel: q and k arrive unnormalised
+ * and each head vector is divided by sqrt(sum x^2 + 1e-6); the gates arrive
+ * raw, as a (in the g slot) and b (in the beta slot), [B, T, Hv] fp32:
+ *
+ *   g_t = -exp(A_log[h]) * softplus(a_t + dt_bias[h]),   beta_t = sigmoid(b_t)
+ *
+ * with A_log, dt_bias [Hv] fp32 per v head, or NULL for zeros (g_t =
+ * -softplus(a_t)).  The pages state only that the projection-side operators
+ * are fused ("Empowering Hybrid Attention Models on NPUs", §7 Implementation:
+ * operator fusion of the projections); this form is the GDN gate with a
+ * per-head decay rate and step bias.  The norms never materialise normalised
+ * tensors: they are folded into the row and column factors the kernels apply
+ * anyway.  Other arguments, the workspace and errors as gdn_chunk_fwd(_ex).
+ * gdn_recurrent_step_prologue is the decode step with the same prologue.
+ */
+gdn_status gdn_chunk_fwd_prologue(const void* q, const void* k, const void* v, const float* a,
+                                  const float* b, const float* A_log, const float* dt_bias,
+                                  const float* h0, void* o, float* hT, int B, int T, int Hqk,
+                                  int Hv, int dk, int dv, int chunk, float scale,
+                                  const int32_t* cu_seqlens, gdn_stream_t stream);
+gdn_status gdn_chunk_fwd_prologue_ex(const void* q, const void* k, const void* v, const float* a,
+                                     const float* b, const float* A_log, const float* dt_bias,
+                                     const float* h0, void* o, float* hT, int B, int T, int Hqk,
+                                     int Hv, int dk, int dv, int chunk, float scale,
+                                     const int32_t* cu_seqlens, void* workspace,
+                                     size_t workspace_bytes, gdn_stream_t stream);
+gdn_status gdn_recurrent_step_prologue(const void* q, const void* k, const void* v,
+                                       const float* a, const float* b, const float* A_log,
+                                       const float* dt_bias, float* h, void* o, int N, int Hqk,
+                                       int Hv, int dk, int dv, float scale, gdn_stream_t stream);
+
+/*
  * Mamba-2 SSD scan - the same chunked scan without the delta rule's erase term
  * ("Exp 2026-07-13 — Linear-Attention Scans on the NPU", §1 and §3: the SSM
  * scan's four matrix stages per chunk - the C B^T gram, the intra-chunk output,

@@ -33,6 +33,9 @@ SIGNATURES = {
     "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
     "gdn_recurrent_step": (_I, _STEP_ARGS),
     "gdn_recurrent_step_f32": (_I, _STEP_ARGS),
+    "gdn_chunk_fwd_prologue": (_I, _FWD_ARGS[:5] + [_P, _P] + _FWD_ARGS[5:]),
+    "gdn_chunk_fwd_prologue_ex": (_I, _FWD_ARGS[:5] + [_P, _P] + _FWD_ARGS[5:-1] + [_P, _SZ, _P]),
+    "gdn_recurrent_step_prologue": (_I, _STEP_ARGS[:5] + [_P, _P] + _STEP_ARGS[5:]),
     "ssd_chunk_fwd": (_I, _FWD_ARGS),
     "ssd_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
     "ssd_chunk_fwd_f32": (_I, _FWD_ARGS),
@@ -129,6 +132,22 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
                       output_final_state, stream, workspace)
 
 
+def gdn_chunk_fwd_prologue(q, k, v, a, b, A_log=None, dt_bias=None, h0=None, o=None, hT=None, *,
+                           chunk: int = 64, scale: Optional[float] = None, cu_seqlens=None,
+                           output_final_state=True, stream=None, workspace=None):
+    """gdn_chunk_fwd with the fused prologue (bf16): q, k unnormalised; raw gates a, b
+    [B, T, Hv] fp32; A_log, dt_bias [Hv] fp32 or None.  g = -exp(A_log) softplus(a +
+    dt_bias), beta = sigmoid(b), q and k divided by sqrt(sum x^2 + 1e-6).  Returns (o, hT)."""
+    dev = q.device
+    Hv = v.shape[2]
+    for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if t is not None:
+            _need(t, name, torch.float32, dev, (Hv,))
+    return _chunk_fwd("gdn", q, k, v, a, b, h0, o, hT, chunk,
+                      k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
+                      output_final_state, stream, workspace, prologue=(A_log, dt_bias))
+
+
 def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: float = 1.0, cu_seqlens=None, output_final_state=True, stream=None,
                   workspace=None):
@@ -141,7 +160,7 @@ def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
 
 
 def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output_final_state,
-               stream, workspace):
+               stream, workspace, prologue=None):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -174,6 +193,17 @@ def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output
         _need(hT, "hT", torch.float32, dev, (N, Hv, dk, dv))
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(hT),
             N, T, Hqk, Hv, dk, dv, chunk, float(scale), _ptr(cu_seqlens))
+    if prologue is not None:
+        if dt != torch.bfloat16:
+            raise TypeError("the fused prologue takes bf16 q, k, v")
+        args = args[:5] + (_ptr(prologue[0]), _ptr(prologue[1])) + args[5:]
+        need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk, cu_seqlens is not None)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, dev)
+        _check(lib.gdn_chunk_fwd_prologue_ex(*args, _ptr(workspace), workspace.numel(),
+                                             _stream_handle(stream, dev)))
+        return o, hT
     if dt == torch.float32:
         _check(getattr(lib, f"{op}_chunk_fwd_f32")(*args, _stream_handle(stream, dev)))
         return o, hT
@@ -196,12 +226,19 @@ def gdn_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = 
                  stream)
 
 
+def gdn_recurrent_step_prologue(q, k, v, a, b, h, A_log=None, dt_bias=None, o=None, *,
+                                scale: Optional[float] = None, stream=None):
+    """One decode token with the fused prologue (bf16; see gdn_chunk_fwd_prologue)."""
+    return _step("gdn", q, k, v, a, b, h, o, k.shape[-1] ** -0.5 if scale is None else scale,
+                 stream, prologue=(A_log, dt_bias))
+
+
 def ssd_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: float = 1.0, stream=None):
     """One decode token of the Mamba-2 SSD recurrence; updates h in place, returns o."""
     return _step("ssd", q, k, v, g, beta, h, o, scale, stream)
 
 
-def _step(op, q, k, v, g, beta, h, o, scale, stream):
+def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None):
     lib = load_library()
     dev = q.device
     dt = q.dtype
@@ -216,6 +253,16 @@ def _step(op, q, k, v, g, beta, h, o, scale, stream):
     if o is None:
         o = torch.empty((N, Hv, dv), dtype=dt, device=dev)
     _need(o, "o", dt, dev, (N, Hv, dv))
+    if prologue is not None:
+        if dt != torch.bfloat16:
+            raise TypeError("the fused prologue takes bf16 q, k, v")
+        for t, name in zip(prologue, ("A_log", "dt_bias")):
+            if t is not None:
+                _need(t, name, torch.float32, dev, (Hv,))
+        _check(lib.gdn_recurrent_step_prologue(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(prologue[0]), _ptr(prologue[1]),
+            _ptr(h), _ptr(o), N, Hqk, Hv, dk, dv, float(scale), _stream_handle(stream, dev)))
+        return o
     fn = getattr(lib, f"{op}_recurrent_step" + ("" if dt == torch.bfloat16 else "_f32"))
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h), _ptr(o), N, Hqk, Hv,
               dk, dv, float(scale), _stream_handle(stream, dev)))

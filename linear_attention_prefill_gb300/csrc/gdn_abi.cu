@@ -103,6 +103,9 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   p->N = B; p->T = T; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->chunk = chunk;
   p->scale = scale;
   p->delta_rule = 1;
+  p->prologue = 0;
+  p->A_log = nullptr;
+  p->dt_bias = nullptr;
   return GDN_OK;
 }
 
@@ -136,6 +139,9 @@ gdn_status check_step(const void* q, const void* k, const void* v, const float* 
   p->q = q; p->k = k; p->v = v; p->g = g; p->beta = beta; p->h = h; p->o = o;
   p->N = N; p->Hqk = Hqk; p->Hv = Hv; p->dk = dk; p->dv = dv; p->scale = scale;
   p->delta_rule = 1;
+  p->prologue = 0;
+  p->A_log = nullptr;
+  p->dt_bias = nullptr;
   return GDN_OK;
 }
 
@@ -262,6 +268,57 @@ gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v
   gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
   if (s != GDN_OK) return s;
   return run_step(p, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- the forward with the fused prologue ---------------------------------------
+gdn_status gdn_chunk_fwd_prologue_ex(const void* q, const void* k, const void* v, const float* a,
+                                     const float* b, const float* A_log, const float* dt_bias,
+                                     const float* h0, void* o, float* hT, int B, int T, int Hqk,
+                                     int Hv, int dk, int dv, int chunk, float scale,
+                                     const int32_t* cu_seqlens, void* workspace,
+                                     size_t workspace_bytes, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, a, b, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  if (!aligned(A_log, 4) || !aligned(dt_bias, 4))
+    return fail(GDN_ERR_INVALID_ARG, "A_log and dt_bias must be 4-byte aligned");
+  p.prologue = 1;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_chunk_fwd_prologue(const void* q, const void* k, const void* v, const float* a,
+                                  const float* b, const float* A_log, const float* dt_bias,
+                                  const float* h0, void* o, float* hT, int B, int T, int Hqk,
+                                  int Hv, int dk, int dv, int chunk, float scale,
+                                  const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_fwd(q, k, v, a, b, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, &p);
+  if (s != GDN_OK) return s;
+  if (!aligned(A_log, 4) || !aligned(dt_bias, 4))
+    return fail(GDN_ERR_INVALID_ARG, "A_log and dt_bias must be 4-byte aligned");
+  p.prologue = 1;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  return fwd_bf16_pooled(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_recurrent_step_prologue(const void* q, const void* k, const void* v,
+                                       const float* a, const float* b, const float* A_log,
+                                       const float* dt_bias, float* h, void* o, int N, int Hqk,
+                                       int Hv, int dk, int dv, float scale, gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, a, b, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  if (!aligned(A_log, 4) || !aligned(dt_bias, 4))
+    return fail(GDN_ERR_INVALID_ARG, "A_log and dt_bias must be 4-byte aligned");
+  p.prologue = 1;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  return run_step(p, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---- the same kernels without the erase term: Mamba-2 SSD ---------------------

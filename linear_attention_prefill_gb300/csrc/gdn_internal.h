@@ -25,7 +25,15 @@ struct FwdParams {
   float scale;
   unsigned* err;      // device error word: bounded waits record a timeout here
   int delta_rule;     // 1: gated delta rule (GDN); 0: no erase term (Mamba-2 SSD scan)
+  // Fused prologue (prologue != 0): q and k arrive unnormalised and are divided by
+  // sqrt(sum x^2 + kNormEps) per head vector; g holds the raw gate a and beta the raw
+  // b, turned into g = -exp(A_log[h]) softplus(a + dt_bias[h]) and beta = sigmoid(b)
+  // (A_log, dt_bias: [Hv] fp32 or nullptr for zeros).
+  int prologue;
+  const float* A_log;
+  const float* dt_bias;
 };
+constexpr float kNormEps = 1e-6f;
 
 // One decode step.
 struct StepParams {
@@ -39,6 +47,9 @@ struct StepParams {
   int N, Hqk, Hv, dk, dv;
   float scale;
   int delta_rule;     // 1: gated delta rule; 0: no erase term (Mamba-2 SSD)
+  int prologue;       // as in FwdParams: raw q, k, gates a (in g) and b (in beta)
+  const float* A_log;
+  const float* dt_bias;
 };
 
 // Workspace of the bf16 forward: one record per (chunk slot, v head), written

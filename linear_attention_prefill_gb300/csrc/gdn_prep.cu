@@ -59,8 +59,8 @@ struct PrepLayout {
   static constexpr int kTw = kAfterTh + (kVinQ ? 0 : (DV / 64) * 8192);  // bf16 [64][64] sw128
   static constexpr int kTu = kTw + 8192;                                   // fp16 [64][64] sw128
   static constexpr int kAd = kTu + 8192;               // fp32 diagonal blocks of A [4][16][16]
-  static constexpr int kVec = kAd + 4 * 256 * 4;       // beta, G, gamma, e, beta*gamma [5][64]
-  static constexpr int kBar = kVec + 5 * kC * 4;       // 5 mbarriers, tmem address, abort flag
+  static constexpr int kVec = kAd + 4 * 256 * 4;  // beta, G, gamma, e, beta*gamma, 1/|k|, 1/|q|
+  static constexpr int kBar = kVec + 7 * kC * 4;  // 5 mbarriers, tmem address, abort flag
   static constexpr int kBytes = kBar + 64;
   static constexpr int kAlloc = kBytes + 1024;         // slack to align the base
   static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kAd % 16 == 0, "alignment");
@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 4)
   float* s_gam = s_G + kC;
   float* s_e = s_gam + kC;
   float* s_bg = s_e + kC;
+  float* s_rk = s_bg + kC;  // 1/|k_r| with the fused prologue, else 1
+  float* s_rq = s_rk + kC;  // 1/|q_r| likewise
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + Lo::kBar);
   uint64_t* bar_v = bar_kq + 1;
   uint64_t* bar_mma = bar_kq + 2;  // grams
@@ -170,10 +172,19 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int r0 = 2 * lane, r1 = 2 * lane + 1;
     const float* gp = p.g + (long long)t0 * p.Hv + hv;
     const float* bp = p.beta + (long long)t0 * p.Hv + hv;
-    const float g0 = r0 < L ? gp[(long long)r0 * p.Hv] : 0.f;
-    const float g1 = r1 < L ? gp[(long long)r1 * p.Hv] : 0.f;
-    const float b0 = r0 < L ? bp[(long long)r0 * p.Hv] : 0.f;
-    const float b1 = r1 < L ? bp[(long long)r1 * p.Hv] : 0.f;
+    float g0 = r0 < L ? gp[(long long)r0 * p.Hv] : 0.f;
+    float g1 = r1 < L ? gp[(long long)r1 * p.Hv] : 0.f;
+    float b0 = r0 < L ? bp[(long long)r0 * p.Hv] : 0.f;
+    float b1 = r1 < L ? bp[(long long)r1 * p.Hv] : 0.f;
+    if (p.prologue) {  // raw gates: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+      const float amul = p.A_log ? expf(p.A_log[hv]) : 1.f;
+      const float abias = p.dt_bias ? p.dt_bias[hv] : 0.f;
+      auto softplus = [](float x) { return x > 20.f ? x : log1pf(expf(x)); };
+      g0 = r0 < L ? -amul * softplus(g0 + abias) : 0.f;
+      g1 = r1 < L ? -amul * softplus(g1 + abias) : 0.f;
+      b0 = r0 < L ? 1.f / (1.f + expf(-b0)) : 0.f;
+      b1 = r1 < L ? 1.f / (1.f + expf(-b1)) : 0.f;
+    }
     float incl = g0 + g1;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -193,9 +204,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     s_beta[r1] = b1;
     s_bg[r0] = p.delta_rule ? b0 * gam0 : 0.f;  // W's column factor: 0 without the erase
     s_bg[r1] = p.delta_rule ? b1 * gam1 : 0.f;
+    s_rk[r0] = s_rk[r1] = s_rq[r0] = s_rq[r1] = 1.f;
     float* gv = ws.gv(slot, hv, p.Hv);  // gamma_last, then gamma of every row
     if (lane == 31) gv[0] = expf(Glast);
-    *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
+    if (!p.prologue) *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
   }
   tc_fence_before();
   __syncthreads();
@@ -216,6 +228,38 @@ __global__ void __launch_bounds__(kThreads, 4)
       *reinterpret_cast<uint4*>(sm + blk * 8192 + rr * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async();
+    __syncthreads();
+  }
+  if (p.prologue) {
+    // fused prologue: 1/sqrt(sum x^2 + eps) of every k and q row (two threads a row,
+    // 8 of its 16-byte chunks each), folded into the factors the later steps apply:
+    // Kt's row factor e, W's column factor beta gamma, and the gamma the output
+    // stage multiplies q rows by
+    const int R = tid >> 1, half = tid & 1;  // R < 64: k row, else q row R - 64
+    const int r = R & (kC - 1);
+    float ss = 0.f;
+    for (int ch = half * (DK / 16); ch < (half + 1) * (DK / 16); ++ch) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(
+          sm + (ch >> 3) * 16384 + (R >= kC ? 8192 : 0) + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+      }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float inv = rsqrtf(ss + kNormEps);
+    if (half == 0) {
+      if (R < kC) {
+        s_rk[r] = inv;
+        s_e[r] *= inv;
+        s_bg[r] *= inv;
+      } else {
+        s_rq[r] = inv;
+        ws.gv(slot, hv, p.Hv)[4 + r] = s_gam[r] * inv;
+      }
+    }
     __syncthreads();
   }
   if (tid == 0 && !*s_abort) {
@@ -252,14 +296,14 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int r = R & (kC - 1), c0 = 32 * h;
     float x[32];
     tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + c0, x);
-    const float Gr = s_G[r], rowf = isP ? p.scale : s_beta[r];
+    const float Gr = s_G[r], rowf = isP ? p.scale * s_rq[r] : s_beta[r] * s_rk[r];
     // last column kept; without the erase term (SSD) A is zero, so Tm = I and U = diag(beta) V
     const int lim = isP ? r : (p.delta_rule ? r - 1 : -1);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int cc = c0 + j;
       const float m = ex2_approx((Gr - s_G[cc]) * kLog2e);
-      x[j] = (cc <= lim && r < L) ? rowf * m * x[j] : 0.f;
+      x[j] = (cc <= lim && r < L) ? rowf * m * s_rk[cc] * x[j] : 0.f;
     }
     if (isP) {
       __half* P = ws.P(slot, hv, p.Hv);

@@ -39,11 +39,44 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
   const TIn* k = static_cast<const TIn*>(p.k) + ((long long)n * p.Hqk + hq) * DK;
   for (int i = tid; i < DK; i += kWarps * 32) {
     sk[i] = to_f(k[i]);
-    sq[i] = to_f(q[i]) * p.scale;
+    sq[i] = to_f(q[i]);
+  }
+  float rk = 1.f, rq = 1.f;
+  if (p.prologue) {  // fused prologue: unit k and q rows (divided by sqrt(sum x^2 + eps))
+    __shared__ float s_inv[2];
+    __syncthreads();
+    if (warp == 0) {
+      float kk = 0.f, qq = 0.f;
+      for (int i = lane; i < DK; i += 32) {
+        kk = fmaf(sk[i], sk[i], kk);
+        qq = fmaf(sq[i], sq[i], qq);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        qq += __shfl_xor_sync(0xffffffffu, qq, off);
+      }
+      if (lane == 0) {
+        s_inv[0] = rsqrtf(kk + kNormEps);
+        s_inv[1] = rsqrtf(qq + kNormEps);
+      }
+    }
+    __syncthreads();
+    rk = s_inv[0];
+    rq = s_inv[1];
+  }
+  for (int i = tid; i < DK; i += kWarps * 32) {  // each thread rescales the entries it loaded
+    sk[i] *= rk;
+    sq[i] *= rq * p.scale;
   }
   const long long nh = (long long)n * p.Hv + hv;
-  const float alpha = expf(p.g[nh]);
-  const float b = p.beta[nh];
+  float gate = p.g[nh], b = p.beta[nh];
+  if (p.prologue) {  // raw gates: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+    const float x = gate + (p.dt_bias ? p.dt_bias[hv] : 0.f);
+    gate = -(p.A_log ? expf(p.A_log[hv]) : 1.f) * (x > 20.f ? x : log1pf(expf(x)));
+    b = 1.f / (1.f + expf(-b));
+  }
+  const float alpha = expf(gate);
   const int col = tile * kCols + lane;
   const float vcol = to_f(static_cast<const TIn*>(p.v)[nh * p.dv + col]);
   __syncthreads();

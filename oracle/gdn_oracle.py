@@ -55,7 +55,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["gdn_dense", "gdn_recurrent", "gdn_chunked", "gdn_step", "chains",
-           "qk_head", "forward_substitution_inverse"]
+           "qk_head", "forward_substitution_inverse", "prologue"]
 
 
 def _f64(x):
@@ -291,3 +291,26 @@ def gdn_chunked(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chunk=64,
                                             g[b, t0:t1, hv], beta[b, t0:t1, hv], h, scale, chunk)
             hT[n, hv] = h
     return o, hT
+
+
+# --------------------------------------------------------------------------
+# The fused prologue's elementwise steps, written out on their own
+# --------------------------------------------------------------------------
+def prologue(q, k, a, b, A_log=None, dt_bias=None, eps=1e-6):
+    """Unnormalised q, k and raw gates -> the inputs the rule takes.
+
+    q_hat = q / sqrt(sum q^2 + eps) per head vector (likewise k);
+    g = -exp(A_log[h]) * softplus(a + dt_bias[h]); beta = 1 / (1 + exp(-b)).
+    A_log, dt_bias: [Hv] or None (zeros).  Returns (q_hat, k_hat, g, beta) in fp64.
+    """
+    q, k, a, b = map(_f64, (q, k, a, b))
+    Hv = a.shape[-1]
+    A_log = np.zeros(Hv) if A_log is None else _f64(A_log)
+    dt_bias = np.zeros(Hv) if dt_bias is None else _f64(dt_bias)
+    qh = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
+    kh = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)
+    x = a + dt_bias
+    softplus = np.where(x > 30.0, x, np.log1p(np.exp(np.minimum(x, 30.0))))
+    g = -np.exp(A_log) * softplus
+    beta = 1.0 / (1.0 + np.exp(-b))
+    return qh, kh, g, beta

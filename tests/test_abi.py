@@ -29,7 +29,9 @@ def test_header_declares_the_boundary():
     for want in ("gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_recurrent_step",
                  "gdn_recurrent_step_f32", "gdn_status_string", "gdn_last_error",
                  "gdn_device_status", "gdn_abi_version", "ssd_chunk_fwd", "ssd_chunk_fwd_ex",
-                 "ssd_chunk_fwd_f32", "ssd_recurrent_step", "ssd_recurrent_step_f32"):
+                 "ssd_chunk_fwd_f32", "ssd_recurrent_step", "ssd_recurrent_step_f32",
+                 "gdn_chunk_fwd_prologue", "gdn_chunk_fwd_prologue_ex",
+                 "gdn_recurrent_step_prologue", "gdn_selftest_expired_wait"):
         assert want in names
 
 
