@@ -1,10 +1,11 @@
 // gdn_common.cuh - device helpers shared by the GDN kernels (sm_103a).
 //
-// Warp-level fp16 tensor-core fragments (mma.sync m16n8k16), ldmatrix loads,
-// cp.async staging, and the blocked unit-lower-triangular inverse used by the
-// #3 Solve operator of the chunkwise form ("Empowering Hybrid Attention Models
-// on NPUs", §2.1, Figure 1(b); the UT transform (I + A)^-1 of "Exp 2026-07-13
-// — Linear-Attention Scans on the NPU", §1).
+// Warp-level tensor-core fragments (mma.sync m16n8k16) and ldmatrix loads,
+// swizzled 16-bit tiles, cp.async, bulk copies and bounded mbarrier waits, and
+// the fp32 blocked unit-lower-triangular inverse of the fp32 path's #3 Solve
+// ("Empowering Hybrid Attention Models on NPUs", §2.1, Figure 1(b); the UT
+// transform (I + A)^-1 of "Exp 2026-07-13 — Linear-Attention Scans on the NPU",
+// §1).  The 5th-generation tensor-core and TMA primitives are in gdn_tc.cuh.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -299,121 +300,19 @@ __device__ __forceinline__ void bf16x8_to_f16x8_scaled(void* p, float scale) {
   *reinterpret_cast<uint4*>(p) = out;
 }
 
-// ---- blocked unit-lower-triangular inverse, 64 x 64 -------------------------
-// T = (I + A)^-1 for strictly lower-triangular A.  The four diagonal 16x16
-// blocks are inverted by forward substitution in fp32 (one warp per block, one
-// lane per column: x_i = [i == l] - sum_{m<i} A_im x_m).  The off-diagonal
-// blocks follow from T_IJ = -T_II (sum_{J<=M<I} A_IM T_MJ), merged on the
-// tensor cores in two levels: 16 -> 32 (blocks (1,0) and (3,2)) and 32 -> 64
-// (rows 32-63 x columns 0-31), each as -(T_II A_IJ) T_JJ with fp16 operands and
-// fp32 accumulation, the first product re-used in registers as the A operand
-// of the second.
-//   A   fp32 [64][lda], strictly lower part read (diagonal blocks)
-//   Ah  fp16 [64][ldh], the same A (off-diagonal blocks read)
-//   T   fp32 [64][ldt], written completely (upper blocks zero)
-//   Th  fp16 [64][ldh], scratch copy of T for the merges
-// Called by all 256 threads (8 warps) of the block; ends with a barrier.
+// C fragments of two adjacent n8 tiles -> the A fragment of one k16 step (fp16).
 __device__ __forceinline__ void c_to_a(uint32_t (&a)[4], const float (&c0)[4], const float (&c1)[4]) {
-  // C fragments of two adjacent n8 tiles -> A fragment of one k16 step
   a[0] = pack_f16(c0[0], c0[1]);
   a[1] = pack_f16(c0[2], c0[3]);
   a[2] = pack_f16(c1[0], c1[1]);
   a[3] = pack_f16(c1[2], c1[3]);
 }
 
-__device__ __forceinline__ void solve_unit_lower_64(const float* A, int lda, const __half* Ah,
-                                                    float* T, int ldt, __half* Th, int ldh) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  if (warp < 4) {
-    if (lane < 16) {
-      const int b = warp, l = lane;
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float s = (i == l) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < i; ++m) s -= A[(16 * b + i) * lda + 16 * b + m] * x[m];
-        x[i] = s;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        T[(16 * b + i) * ldt + 16 * b + l] = x[i];
-        Th[(16 * b + i) * ldh + 16 * b + l] = __float2half_rn(x[i]);
-      }
-    }
-  } else {
-    for (int e = tid - 128; e < 64 * 64; e += 128) {  // strictly upper blocks
-      const int r = e >> 6, c = e & 63;
-      if ((c >> 4) > (r >> 4)) {
-        T[r * ldt + c] = 0.f;
-        Th[r * ldh + c] = __float2half_rn(0.f);
-      }
-    }
-  }
-  __syncthreads();
-  // level 1: T10 = -(T11 A10) T00 (warp 0), T32 = -(T33 A32) T22 (warp 1)
-  if (warp < 2) {
-    const int i0 = 16 + 32 * warp, j0 = 32 * warp;  // block rows i0.., columns j0..
-    float y[2][4] = {}, t[2][4] = {};
-    uint32_t a[4], b[4];
-    load_a(a, Th, ldh, i0, i0, lane);       // T_II
-    load_b_kn(b, Ah, ldh, j0, i0, lane);    // A_IJ as [k][n]
-    mma_f16(y[0], a, b[0], b[1]);
-    mma_f16(y[1], a, b[2], b[3]);
-    c_to_a(a, y[0], y[1]);
-    load_b_kn(b, Th, ldh, j0, j0, lane);    // T_JJ as [k][n]
-    mma_f16(t[0], a, b[0], b[1]);
-    mma_f16(t[1], a, b[2], b[3]);
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int r = i0 + gq + ((x >> 1) << 3), c = j0 + 8 * jn + 2 * tq + (x & 1);
-        T[r * ldt + c] = -t[jn][x];
-        Th[r * ldh + c] = __float2half_rn(-t[jn][x]);
-      }
-  }
-  __syncthreads();
-  // level 2: rows 32..63 x columns 0..31 = -(T_BB A_BA) T_AA; warp w < 2 takes 16 rows
-  if (warp < 2) {
-    const int i0 = 32 + 16 * warp;
-    float y[4][4] = {}, t[4][4] = {};
-    uint32_t a[4], b[4];
-    for (int k0 = 32; k0 <= i0; k0 += 16) {  // T_BB is lower triangular
-      load_a(a, Th, ldh, i0, k0, lane);
-      load_b_kn(b, Ah, ldh, 0, k0, lane);
-      mma_f16(y[0], a, b[0], b[1]);
-      mma_f16(y[1], a, b[2], b[3]);
-      load_b_kn(b, Ah, ldh, 16, k0, lane);
-      mma_f16(y[2], a, b[0], b[1]);
-      mma_f16(y[3], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {            // k over the 32 columns of Y
-      c_to_a(a, y[2 * s], y[2 * s + 1]);
-      load_b_kn(b, Th, ldh, 0, 16 * s, lane);
-      mma_f16(t[0], a, b[0], b[1]);
-      mma_f16(t[1], a, b[2], b[3]);
-      load_b_kn(b, Th, ldh, 16, 16 * s, lane);
-      mma_f16(t[2], a, b[0], b[1]);
-      mma_f16(t[3], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int jn = 0; jn < 4; ++jn)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int r = i0 + gq + ((x >> 1) << 3), c = 8 * jn + 2 * tq + (x & 1);
-        T[r * ldt + c] = -t[jn][x];
-      }
-  }
-  __syncthreads();
-}
-
 // ---- blocked unit-lower-triangular inverse, 64 x 64, all fp32 (SIMT) -----------
-// The same blocked scheme with every product in fp32 on the CUDA cores, for the
-// fp32 path: diagonal 16x16 blocks by forward substitution, then block row by
-// block row T_IJ = -T_II * sum_{J<=M<I} A_IM T_MJ.  Called by all NTHREADS
+// T = (I + A)^-1 for strictly lower-triangular A, every product in fp32 on the
+// CUDA cores, for the fp32 path: diagonal 16x16 blocks by forward substitution
+// (x_i = [i == l] - sum_{m<i} A_im x_m), then block row by block row
+// T_IJ = -T_II * sum_{J<=M<I} A_IM T_MJ.  Called by all NTHREADS
 // (>= 256) threads; X is 3*256 floats of scratch; ends with a barrier.
 template <int NTHREADS>
 __device__ __forceinline__ void solve_unit_lower_64_f32(const float* A, int lda, float* T, int ldt,
