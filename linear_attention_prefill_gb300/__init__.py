@@ -5,12 +5,12 @@ package holds the Python binding with the ABI's names, the seeded synthetic
 workloads and the algorithmic byte/FLOP model.  The same kernels also run the
 Mamba-2 SSD scan (the recurrence without the delta rule's erase term).
 """
-from .binding import (GdnError, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_prologue,
+from .binding import (GdnError, HostPipeline, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_prologue,
                       gdn_chunk_fwd_workspace_size, gdn_recurrent_step_prologue,
                       gdn_device_status, gdn_recurrent_step, gdn_selftest_expired_wait,
                       load_library, ssd_chunk_fwd, ssd_recurrent_step, status_string)
 
-__all__ = ["GdnError", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_prologue",
+__all__ = ["GdnError", "HostPipeline", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_prologue",
            "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step_prologue",
            "gdn_device_status", "gdn_recurrent_step", "gdn_selftest_expired_wait", "load_library",
            "ssd_chunk_fwd",

@@ -306,9 +306,16 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         d[name] = buf
         nbytes_in += t.numel() * t.element_size()
     fwd = ssd_chunk_fwd if op == "ssd" else gdn_chunk_fwd
+    if "workspace" not in bufs:
+        B, T, Hqk, dk = d["q"].shape
+        Hv, dv = d["v"].shape[2], d["v"].shape[3]
+        N = d["cu_seqlens"].numel() - 1 if d["cu_seqlens"] is not None else B
+        need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk,
+                                            d["cu_seqlens"] is not None)
+        bufs["workspace"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     o_dev, hT_dev = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], bufs.get("o"),
                         bufs.get("hT"), chunk=chunk, cu_seqlens=d["cu_seqlens"], stream=stream,
-                        workspace=bufs.get("workspace"))
+                        workspace=bufs["workspace"])
     bufs["o"], bufs["hT"] = o_dev, hT_dev
     if out is not None and "o_host" in out:
         o_h, hT_h = out["o_host"], out["hT_host"]
@@ -321,3 +328,33 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
     hT_h.copy_(hT_dev, non_blocking=True)
     nbytes_out = o_h.numel() * o_h.element_size() + hT_h.numel() * hT_h.element_size()
     return o_h, hT_h, nbytes_in, nbytes_out
+
+
+class HostPipeline:
+    """Forward calls streamed from pinned host memory, copies overlapped across calls.
+
+    Each call copies its inputs host -> device, runs the forward and copies o and
+    hT device -> host, all on one of ``depth`` streams with its own device buffers,
+    workspace and pinned outputs; consecutive calls go to different streams, so the
+    upload of call i + 1 overlaps the compute and the download of call i (the host
+    link carries one direction of each at once).  ``submit`` returns the pinned
+    (o, hT) of that call and a CUDA event that completes when they are filled.
+    """
+
+    def __init__(self, chunk: int = 64, device="cuda", op: str = "gdn", depth: int = 2):
+        self.dev = torch.device(device)
+        self.chunk, self.op = chunk, op
+        self.slots = [dict(stream=torch.cuda.Stream(self.dev), bufs={}) for _ in range(depth)]
+        self.n = 0
+
+    def submit(self, inputs: dict):
+        slot = self.slots[self.n % len(self.slots)]
+        self.n += 1
+        bufs = slot["bufs"]
+        with torch.cuda.stream(slot["stream"]):
+            o_h, hT_h, nbytes_in, nbytes_out = gdn_chunk_fwd_host(
+                inputs, chunk=self.chunk, device=self.dev, stream=slot["stream"], out=bufs,
+                op=self.op)
+            done = torch.cuda.Event()
+            done.record(slot["stream"])
+        return o_h, hT_h, done, nbytes_in, nbytes_out
