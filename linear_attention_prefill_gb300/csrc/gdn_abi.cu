@@ -3,6 +3,7 @@
 // Validates arguments, maps them onto launch parameters and enqueues the kernels
 // on the caller's stream.  It owns no tensors and allocates nothing.
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -19,6 +20,14 @@ __device__ unsigned long long g_gdn_phase[64];
 namespace gdn {
 
 __device__ unsigned g_device_error = 0u;
+
+bool block_path_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("GDN_BLOCK_PATH");
+    return v && v[0] == '1' && v[1] == 0;
+  }();
+  return on;
+}
 
 cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
   unsigned zero = 0u;
@@ -177,6 +186,15 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
 gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
   cudaError_t e = gdn::launch_prep(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
+  if (w.blocks) {  // dk = dv = 128, gated delta rule: 128-token blocks
+    e = gdn::launch_pair(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the pair kernel");
+    e = gdn::launch_scan(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the scan kernel");
+    e = gdn::launch_out(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the output kernel");
+    return GDN_OK;
+  }
   e = gdn::launch_chain(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the chain kernel");
   return GDN_OK;

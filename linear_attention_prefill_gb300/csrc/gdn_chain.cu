@@ -45,10 +45,10 @@ struct ChainLayout {
   // 1024-byte alignment the swizzle needs, then the workspace record pieces
   static constexpr int kQ = 0;
   static constexpr int kWt = kQ + kC * DK * 2;   // W^T [DK][64] swz<64>
-  static constexpr int kKt = kWt + kC * DK * 2;  // Kt [64][DK] swz<DK>
+  static constexpr int kKt = kWt + kC * DK * 2;  // Kt [64][DK] swzb<64>
   static constexpr int kP = kKt + kC * DK * 2;   // P [64][64] swz<64>
-  static constexpr int kUt = kP + kC * kC * 2;   // U^T [DVT][64]
-  static constexpr int kGv = kUt + DVT * kC * 2; // gamma_last, pad, gamma[64]
+  static constexpr int kUt = kP + kC * kC * 2;   // U^T [DVT][64] swz<64>
+  static constexpr int kGv = kUt + DVT * kC * 2; // gamma_last, pad, gamma[64], e[64]
   static constexpr int kStageBytes = (kGv + kGvFloats * 4 + 1023) / 1024 * 1024;
   static constexpr int kH = kStages * kStageBytes;      // [kPub][DK][DVT] fp16 swz<DVT>
   static constexpr int kVn = kH + kPub * DK * DVT * 2;  // [kPub][64][DVT] fp16 swz<DVT>
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ks = 0; ks < kC / 16; ++ks)
 #pragma unroll
       for (int mt = 0; mt < MTW; ++mt)
-        load_a_trans_sw<DK>(ka[ks][mt], Kt, 16 * (MTW * warp + mt), 16 * ks, lane);
+        load_a_trans_blk<kC>(ka[ks][mt], Kt, 16 * (MTW * warp + mt), 16 * ks, lane);
 
     // #5 read: V_new = U - W h   (warp: 16 token rows x the dv tile)
     const int r0 = 16 * warp + gq;
@@ -301,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int col = 8 * j + 2 * tq;
-        const float2 u0 = make_float2(__half2float(Ut[col * kC + r0]),
-                                      __half2float(Ut[(col + 1) * kC + r0]));
-        const float2 u1 = make_float2(__half2float(Ut[col * kC + r0 + 8]),
-                                      __half2float(Ut[(col + 1) * kC + r0 + 8]));
+        const float2 u0 = make_float2(__half2float(Ut[swz<kC>(col, r0)]),
+                                      __half2float(Ut[swz<kC>(col + 1, r0)]));
+        const float2 u1 = make_float2(__half2float(Ut[swz<kC>(col, r0 + 8)]),
+                                      __half2float(Ut[swz<kC>(col + 1, r0 + 8)]));
         *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0, col)]) =
             pack_f16(u0.x - wh[0][j][0] - wh[1][j][0], u0.y - wh[0][j][1] - wh[1][j][1]);
         *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0 + 8, col)]) =

@@ -162,6 +162,15 @@ __device__ __forceinline__ int swz(int r, int col) {
   return r * W + (pc << 3) + (col & 7);
 }
 
+// Blocked 128-byte swizzle for tiles wider than 64 halves: 64-column blocks of
+// ROWS rows each, stored one after another, every block laid out as swz<64>.
+// This is the tensor cores' 128-byte-swizzled operand layout, for K-major and
+// MN-major use alike.
+template <int ROWS>
+__host__ __device__ __forceinline__ int swzb(int r, int col) {
+  return (col >> 6) * (ROWS * 64) + r * 64 + (((((col & 63) >> 3) ^ r) & 7) << 3) + (col & 7);
+}
+
 // mbarrier arrive (release), one count.
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -259,6 +268,16 @@ __device__ __forceinline__ void load_b_kn_sw(uint32_t (&b)[4], const __half* bas
   const int g = lane >> 3;
   ldsm_x4_t(b[0], b[1], b[2], b[3],
             base + swz<W>(k0 + (lane & 7) + ((g & 1) << 3), n0 + ((g >> 1) << 3)));
+}
+
+// A fragment of a tile stored transposed ([k][m], m contiguous) in the blocked
+// layout swzb<ROWS> (ROWS = number of k rows).
+template <int ROWS>
+__device__ __forceinline__ void load_a_trans_blk(uint32_t (&a)[4], const __half* base, int m0,
+                                                 int k0, int lane) {
+  const int g = lane >> 3;
+  ldsm_x4_t(a[0], a[1], a[2], a[3],
+            base + swzb<ROWS>(k0 + (lane & 7) + ((g >> 1) << 3), m0 + ((g & 1) << 3)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

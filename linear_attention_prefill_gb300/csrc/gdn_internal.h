@@ -57,11 +57,15 @@ struct StepParams {
 // 16-byte chunks XOR-swizzled per row (gdn::swz<width>), so a verbatim bulk
 // copy lands in shared memory ready for conflict-free ldmatrix:
 //   W    [dk][64]   W^T, W = Tm diag(beta gamma) K, swz<64>, fp16
-//   Kt   [64][dk]   diag(e) K, e_j = exp(G_last - G_j), swz<dk>, fp16
+//   Kt   [64][dk]   diag(e) K, e_j = exp(G_last - G_j), swzb<64> (64-column
+//                   blocks), fp16
 //   P    [64][64]   tril(scale exp(G_i - G_j) q_i.k_j), swz<64>, fp16
-//   U    [dv][64]   U^T, U = Tm diag(beta) V, fp16, not swizzled: the t-column
-//                   dv tile j is the contiguous rows [j t, (j + 1) t)
-//   gv   fp32 [68]  gamma_last, 3 pad, gamma_i = exp(G_i) for the 64 rows
+//   U    [dv][64]   U^T, U = Tm diag(beta) V, swz<64>, fp16: the t-column dv
+//                   tile j is the contiguous rows [j t, (j + 1) t)
+//   gv   fp32 [132] gamma_last, 3 pad, gamma_i = exp(G_i) for the 64 rows, then
+//                   e_j for the 64 rows (norm factors folded in with the prologue)
+// Every 16-bit tile is in the tensor cores' 128-byte-swizzled layout, so the
+// same bytes serve ldmatrix loads and tcgen05 operand descriptors.
 // The dv tile t (16 or 32 columns, one chain CTA each) is picked per call by
 // dv_tile(): the narrowest that still leaves at most ~one CTA per SM, since
 // every chain CTA must take in the whole W, Kt, P and q of each chunk.
@@ -70,7 +74,19 @@ struct StepParams {
 // overlaps because floor((a + L) / 64) - floor(a / 64) + 1 >= ceil(L / 64), and
 // ends below floor(T / 64) + N + 1.
 constexpr int kChunk = 64;
-constexpr int kGvFloats = 68;
+constexpr int kGvFloats = 132;
+
+// The block path (gdn_pair.cu; gated delta rule, dk = dv = 128) adds one pair
+// record per (128-token block slot, v head) after the chunk records: block b of
+// a sequence is its chunks 2b and 2b + 1, and its record holds
+//   N    [2][dk][64]     N = Kb^T Wb, the block's state transition h <- gamma h
+//                        - N h + B (swzb<dk>, fp16; K-major over the input dk)
+//   B    [dv/64][dk][64] B = Kb^T Ub (swzb<dk>, fp16)
+//   H    [dv/64][dk][64] the fp16 state entering the block (swzb<dk>)
+//   gp   fp32            gamma_last of the block (16 bytes)
+// Block slots follow the chunk slots' rule with 128 tokens: n * ceil(T / 128),
+// or floor(cu[n] / 128) + n.
+constexpr int kBlock = 128;
 
 struct WsLayout {
   char* base;
@@ -78,6 +94,28 @@ struct WsLayout {
   long long n_slots;        // chunk slots per v head
   long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
   long long task_bytes, kt_off, p_off, u_off, gv_off;
+  int blocks;               // 1: the block path runs (pair records present)
+  long long n_bslots, bslots_per_seq, pair_off, pair_bytes, pb_off, ph_off, pg_off;
+
+  __host__ __device__ char* prec(long long bslot, int hv, int Hv) const {
+    return base + pair_off + (bslot * Hv + hv) * pair_bytes;
+  }
+  __host__ __device__ __half* PN(long long b, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(prec(b, hv, Hv));
+  }
+  __host__ __device__ __half* PB(long long b, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(prec(b, hv, Hv) + pb_off);
+  }
+  __host__ __device__ __half* PH(long long b, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(prec(b, hv, Hv) + ph_off);
+  }
+  __host__ __device__ float* PG(long long b, int hv, int Hv) const {
+    return reinterpret_cast<float*>(prec(b, hv, Hv) + pg_off);
+  }
+  __device__ long long first_bslot(const FwdParams& p, int n) const {
+    if (p.cu_seqlens) return (long long)(p.cu_seqlens[n] / kBlock) + n;
+    return (long long)n * bslots_per_seq;
+  }
 
   __host__ __device__ char* rec(long long slot, int hv, int Hv) const {
     return base + (slot * Hv + hv) * task_bytes;
@@ -111,6 +149,10 @@ inline int dv_tile(const FwdParams& p) {
   return 32;
 }
 
+// Whether the 128-token block path (gdn_block.cu) runs for the shapes it covers:
+// on when the environment variable GDN_BLOCK_PATH is "1" at first use (gdn_abi.cu).
+bool block_path_enabled();
+
 // Layout for one call (sizes validated); base may be null when only sizing.
 inline WsLayout ws_layout(const FwdParams& p, void* base) {
   WsLayout w;
@@ -129,9 +171,24 @@ inline WsLayout ws_layout(const FwdParams& p, void* base) {
   w.u_off = w.p_off + (long long)kChunk * kChunk * 2;
   w.gv_off = w.u_off + wv;
   w.task_bytes = (w.gv_off + kGvFloats * 4 + 127) / 128 * 128;  // records on 128-byte lines
+  w.blocks = p.delta_rule && p.dk == 128 && p.dv == 128 && block_path_enabled();
+  if (p.cu_seqlens) {
+    w.bslots_per_seq = 0;
+    w.n_bslots = (long long)p.T / kBlock + p.N + 1;
+  } else {
+    w.bslots_per_seq = ((long long)p.T + kBlock - 1) / kBlock;
+    w.n_bslots = w.bslots_per_seq * p.N;
+  }
+  w.pair_off = w.n_slots * p.Hv * w.task_bytes;
+  w.pb_off = (long long)p.dk * p.dk * 2;
+  w.ph_off = w.pb_off + (long long)p.dk * p.dv * 2;
+  w.pg_off = w.ph_off + (long long)p.dk * p.dv * 2;
+  w.pair_bytes = w.blocks ? (w.pg_off + 16 + 127) / 128 * 128 : 0;
   return w;
 }
-inline size_t ws_bytes(const WsLayout& w, int Hv) { return (size_t)(w.n_slots * Hv * w.task_bytes); }
+inline size_t ws_bytes(const WsLayout& w, int Hv) {
+  return (size_t)(w.n_slots * Hv * w.task_bytes + w.n_bslots * Hv * w.pair_bytes);
+}
 
 // Slot -> (sequence, chunk of that sequence); false for a slot no chunk uses.
 __device__ inline bool locate_chunk(const FwdParams& p, const WsLayout& ws, long long slot, int* n,
@@ -154,6 +211,27 @@ __device__ inline bool locate_chunk(const FwdParams& p, const WsLayout& ws, long
   return true;
 }
 
+// Block slot -> (sequence, block of that sequence); false for a slot no block uses.
+__device__ inline bool locate_block(const FwdParams& p, const WsLayout& ws, long long bslot, int* n,
+                                    int* b) {
+  if (!p.cu_seqlens) {
+    *n = (int)(bslot / ws.bslots_per_seq);
+    *b = (int)(bslot % ws.bslots_per_seq);
+    return *n < p.N;
+  }
+  int lo = 0, hi = p.N - 1;  // largest n with first_bslot(n) <= bslot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)(p.cu_seqlens[mid] / kBlock) + mid <= bslot) lo = mid; else hi = mid - 1;
+  }
+  const long long first = (long long)(p.cu_seqlens[lo] / kBlock) + lo;
+  const long long len = (long long)p.cu_seqlens[lo + 1] - p.cu_seqlens[lo];
+  if (bslot < first || bslot - first >= (len + kBlock - 1) / kBlock) return false;
+  *n = lo;
+  *b = (int)(bslot - first);
+  return true;
+}
+
 // Tensor map of a row-major [rows, cols] bf16 matrix, boxes of 64 x 64 with the
 // 128-byte swizzle (gdn_prep.cu); false if the driver refuses it.
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols);
@@ -161,6 +239,10 @@ bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long
 // Launchers: return cudaSuccess or the launch error.  Each validates nothing.
 cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+// The block path (ws.blocks): pair transitions, the block scan, the block output.
+cudaError_t launch_pair(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+cudaError_t launch_scan(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+cudaError_t launch_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream);
 cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream);

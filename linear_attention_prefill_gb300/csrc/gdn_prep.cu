@@ -207,7 +207,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     s_rk[r0] = s_rk[r1] = s_rq[r0] = s_rq[r1] = 1.f;
     float* gv = ws.gv(slot, hv, p.Hv);  // gamma_last, then gamma of every row
     if (lane == 31) gv[0] = expf(Glast);
-    if (!p.prologue) *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
+    if (!p.prologue) {
+      *reinterpret_cast<float2*>(gv + 4 + r0) = make_float2(gam0, gam1);
+      *reinterpret_cast<float2*>(gv + 68 + r0) = make_float2(s_e[r0], s_e[r1]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -255,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         s_rk[r] = inv;
         s_e[r] *= inv;
         s_bg[r] *= inv;
+        ws.gv(slot, hv, p.Hv)[68 + r] = s_e[r];
       } else {
         s_rq[r] = inv;
         ws.gv(slot, hv, p.Hv)[4 + r] = s_gam[r] * inv;
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     for (int i = tid; i < kC * kRowChunks; i += kThreads) {
       const int r = i / kRowChunks, ch = i % kRowChunks;
       const unsigned char* src = sm + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(Kt + swz<DK>(r, ch * 8)) = scale_bf16x8_to_f16(src, s_e[r]);
+      *reinterpret_cast<uint4*>(Kt + swzb<kC>(r, ch * 8)) = scale_bf16x8_to_f16(src, s_e[r]);
     }
   }
   GDN_STAMP(33, 0);  // Kt written (thread 0's share)
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       __half* Ut = ws.U(slot, hv, p.Hv);  // [dv][64], plain
 #pragma unroll
       for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<uint4*>(Ut + d * kC + 32 * h + 8 * m) = pack8_f16(x + 8 * m);
+        *reinterpret_cast<uint4*>(Ut + swz<kC>(d, 32 * h + 8 * m)) = pack8_f16(x + 8 * m);
     }
   }
   GDN_PHASE(4);  // W/U
