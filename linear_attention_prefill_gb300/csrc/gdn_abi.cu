@@ -187,6 +187,11 @@ gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cuda
   cudaError_t e = gdn::launch_prep(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
   if (w.blocks) {  // dk = dv = 128, gated delta rule: 128-token blocks
+    if (gdn::scan_out_fused(p)) {  // pair, scan and output work in one launch
+      e = gdn::launch_scan_out(p, w, stream, true);
+      if (e != cudaSuccess) return cuda_fail(e, "launching the block kernel");
+      return GDN_OK;
+    }
     e = gdn::launch_pair(p, w, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launching the pair kernel");
     e = gdn::launch_scan(p, w, stream);

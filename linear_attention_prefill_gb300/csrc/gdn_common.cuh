@@ -81,6 +81,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
+// Count `bytes` of the current phase's expected transactions as done, without
+// any copy (releases a barrier whose copy was not issued).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
 // Arrive once and add `bytes` to the transaction count of the current phase.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),

@@ -96,6 +96,18 @@ struct WsLayout {
   long long task_bytes, kt_off, p_off, u_off, gv_off;
   int blocks;               // 1: the block path runs (pair records present)
   long long n_bslots, bslots_per_seq, pair_off, pair_bytes, pb_off, ph_off, pg_off;
+  // fused scan launch: [n_bslots][Hv] pair-done flags, [n_bslots][Hv][2]
+  // stored-state flags, then the task counter (zeroed before each launch)
+  long long flag_off, flag_bytes;
+  int hv_count;
+
+  __host__ __device__ unsigned* pair_flags() const {
+    return reinterpret_cast<unsigned*>(base + flag_off);
+  }
+  __host__ __device__ unsigned* scan_flags() const { return pair_flags() + n_bslots * hv_count; }
+  __host__ __device__ unsigned* task_counter() const {
+    return pair_flags() + n_bslots * hv_count * 3;
+  }
 
   __host__ __device__ char* prec(long long bslot, int hv, int Hv) const {
     return base + pair_off + (bslot * Hv + hv) * pair_bytes;
@@ -184,10 +196,13 @@ inline WsLayout ws_layout(const FwdParams& p, void* base) {
   w.ph_off = w.pb_off + (long long)p.dk * p.dv * 2;
   w.pg_off = w.ph_off + (long long)p.dk * p.dv * 2;
   w.pair_bytes = w.blocks ? (w.pg_off + 16 + 127) / 128 * 128 : 0;
+  w.hv_count = p.Hv;
+  w.flag_off = w.pair_off + w.n_bslots * p.Hv * w.pair_bytes;
+  w.flag_bytes = w.blocks ? (w.n_bslots * p.Hv * 3 * 4 + 4 + 127) / 128 * 128 : 0;
   return w;
 }
 inline size_t ws_bytes(const WsLayout& w, int Hv) {
-  return (size_t)(w.n_slots * Hv * w.task_bytes + w.n_bslots * Hv * w.pair_bytes);
+  return (size_t)(w.n_slots * Hv * w.task_bytes + w.n_bslots * Hv * w.pair_bytes + w.flag_bytes);
 }
 
 // Slot -> (sequence, chunk of that sequence); false for a slot no chunk uses.
@@ -235,6 +250,10 @@ __device__ inline bool locate_block(const FwdParams& p, const WsLayout& ws, long
 // Tensor map of a row-major [rows, cols] bf16 matrix, boxes of 64 x 64 with the
 // 128-byte swizzle (gdn_prep.cu); false if the driver refuses it.
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, long long rows, long long cols);
+// Tensor map of a row-major [planes, rows, cols] bf16 tensor, boxes of 64 x 64 x 1
+// with the 128-byte swizzle; a store clips at each plane's `rows`.
+bool make_tensor_map_bf16_3d(CUtensorMap* m, const void* base, long long planes, long long rows,
+                             long long cols);
 
 // Launchers: return cudaSuccess or the launch error.  Each validates nothing.
 cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
@@ -243,6 +262,11 @@ cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t st
 cudaError_t launch_pair(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_scan(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+// The scan and the block output in one launch (fixed-length rows, few enough
+// chains to leave SMs for the output work); scan_out_fused says when.
+bool scan_out_fused(const FwdParams& p);
+cudaError_t launch_scan_out(const FwdParams& p, const WsLayout& ws, cudaStream_t stream,
+                            bool pairs);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream);
 cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream);
