@@ -29,6 +29,13 @@
  *  - Errors: a non-OK status means nothing was launched (except GDN_ERR_CUDA,
  *    which reports a failed launch).  gdn_last_error() gives a one-line
  *    description, per calling thread.  Nothing prints, aborts or throws.
+ *  - Environment: GDN_BLOCK_PATH=1, read once when the library is first used,
+ *    runs the bf16 gated-delta-rule forward at dk = dv = 128 on 128-token
+ *    blocks (two chunks' state maps composed into one, the state walked with
+ *    one tensor-core product per block, the block outputs in parallel); the
+ *    result is the same function within the same tolerances, and
+ *    gdn_chunk_fwd_workspace_size grows accordingly.  Unset (the default), the
+ *    forward walks 64-token chunks, which is faster on GB300.
  */
 #ifndef GDN_H_
 #define GDN_H_

@@ -26,14 +26,17 @@
 // identities of "Exp 2026-07-13 — Linear-Attention Scans on the NPU", §1,
 // applied to a chunk of twice the length.
 //
-// Three launches:
-//   gdn_pair_kernel  (block, v head): X, W2', U2' (written back into the second
-//                    chunk's record), N, B, gamma -> the block record
-//   gdn_scan_kernel  (sequence, v head, 64-column dv tile): walks the blocks in
-//                    order, fp32 state tile in registers, one M = 128, N = 64,
-//                    K = 128 tcgen05 product per block; stores the fp16 state
-//                    entering each block
-//   gdn_out_kernel   (block, v head): V_new, Y, then O in one accumulator
+// Three stages, as three launches or (fixed-length rows) one:
+//   pair task   (block, v head): X, W2', U2' (written back into the second
+//               chunk's record), N, B, gamma -> the block record
+//   scan chain  (sequence, v head, 64-column dv tile): walks the blocks in
+//               order, fp32 state tile in registers, one M = 128, N = 64,
+//               K = 128 tcgen05 product per block; stores the fp16 state
+//               entering each block
+//   out task    (block, v head): V_new, Y, then O in one accumulator
+// gdn_pair_kernel, gdn_scan_kernel and gdn_out_kernel run one stage each;
+// gdn_scanout_kernel runs the scan chains beside worker CTAs that take the
+// pair and out tasks in block order, synchronised by per-block flags.
 // All products are tcgen05 (kind::f16, fp32 accumulation in tensor memory) on
 // 128-byte-swizzled shared-memory operands; tiles arrive by bulk copy or TMA.
 #include "gdn_common.cuh"
