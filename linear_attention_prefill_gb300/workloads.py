@@ -15,6 +15,7 @@ state per head, §5 "adding a 64-KiB state"):
 * v ~ N(0, 1) rounded to the input dtype;
 * beta = sigmoid(N(0, 1)) in fp32 (already squashed: the kernel takes beta);
 * g = -softplus(N(mu, 1)) * s in fp32 (a log-decay <= 0; mu and s per workload);
+  for Kimi Delta Attention (op "kda") one such draw per key channel, g [B, T, Hv, dk];
 * h0 ~ N(0, sigma) in fp32 where a workload carries state, else absent.
 
 All draws come from one ``torch.Generator`` seeded per workload, on the device
@@ -45,7 +46,8 @@ class Workload:
     g_mu: float = 0.0       # g = -softplus(N(g_mu, 1)) * g_scale
     g_scale: float = 1.0
     h0_std: Optional[float] = None   # None: no initial state (zeros)
-    op: str = "gdn"                  # "gdn" (gated delta rule) or "ssd" (Mamba-2 scan)
+    op: str = "gdn"                  # "gdn" (gated delta rule), "ssd" (Mamba-2 scan) or
+                                     # "kda" (delta rule with a per-channel gate)
     varlen: bool = False    # True: one packed [1, T_total, ...] batch with cu_seqlens
     seed: int = 0
     decode_steps: int = 0   # one-token steps that continue from the final state
@@ -60,7 +62,7 @@ class Workload:
 
     @property
     def scale(self) -> float:
-        return float(self.dk) ** -0.5 if self.op == "gdn" else 1.0
+        return 1.0 if self.op == "ssd" else float(self.dk) ** -0.5
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -99,6 +101,11 @@ WORKLOADS["long_64k_weak_c128"] = WORKLOADS["long_64k_weak"].replace(
 WORKLOADS["ssd_80h_4k"] = Workload("ssd_80h_4k", (4096,), 1, 80, 128, 64, 64, "bf16", seed=6,
                                    op="ssd")
 
+# Kimi Delta Attention layer (the pages' KDA kernels at 16 heads, Figure 13; head dim 128 and
+# the per-channel fp32 gate of Figure 4), 4K prompt.
+WORKLOADS["kda_16h_4k"] = Workload("kda_16h_4k", (4096,), 16, 16, 128, 128, 64, "bf16", seed=7,
+                                   op="kda")
+
 # The workload the headline throughput is quoted on.
 HEADLINE = "layer_16h_4k"
 
@@ -120,8 +127,8 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
     """Draw one batch of inputs for workload ``w`` on ``device``.
 
-    Returns a dict with q, k ([B, T, Hqk, dk]), v ([B, T, Hv, dv]), g, beta
-    ([B, T, Hv] fp32), h0 ([N, Hv, dk, dv] fp32 or None), cu_seqlens (int32
+    Returns a dict with q, k ([B, T, Hqk, dk]), v ([B, T, Hv, dv]), g ([B, T, Hv]
+    fp32, or [B, T, Hv, dk] for KDA), beta ([B, T, Hv] fp32), h0 ([N, Hv, dk, dv] fp32 or None), cu_seqlens (int32
     [N+1] on ``device`` for varlen workloads, else None), and the sizes
     B, T, N, scale.  A varlen batch is one packed row: B = N sequences,
     tensors [1, T_total, ...].
@@ -147,6 +154,9 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
         # per head
         beta = torch.nn.functional.softplus(randn(B, T, w.Hv))
         g = -beta * torch.exp(0.3 * randn(w.Hv))
+    elif w.op == "kda":
+        beta = torch.sigmoid(randn(B, T, w.Hv))
+        g = -torch.nn.functional.softplus(randn(B, T, w.Hv, w.dk) + w.g_mu) * w.g_scale
     else:
         beta = torch.sigmoid(randn(B, T, w.Hv))
         g = -torch.nn.functional.softplus(randn(B, T, w.Hv) + w.g_mu) * w.g_scale
@@ -176,6 +186,9 @@ def make_decode_inputs(w: Workload, step: int, device="cpu") -> dict:
     if w.op == "ssd":
         beta = torch.nn.functional.softplus(randn(N, w.Hv))
         g = -beta * torch.exp(0.3 * randn(w.Hv))
+    elif w.op == "kda":
+        beta = torch.sigmoid(randn(N, w.Hv))
+        g = -torch.nn.functional.softplus(randn(N, w.Hv, w.dk) + w.g_mu) * w.g_scale
     else:
         beta = torch.sigmoid(randn(N, w.Hv))
         g = -torch.nn.functional.softplus(randn(N, w.Hv) + w.g_mu) * w.g_scale
