@@ -242,6 +242,47 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
                                   gdn_stream_t stream);
 
 /*
+ * Kimi Delta Attention (KDA) - the delta rule with a per-key-channel gate.
+ * "Empowering Hybrid Attention Models on NPUs" runs GDN and KDA through the same
+ * Map-Reduce-Map chunkwise paradigm (§2.1, Figure 1); KDA's gate is one fp32
+ * log-decay per token, head and key channel (Figure 4(a) prices it at 31.33 MiB
+ * against GDN's 21.41 MiB at T = 2048, H = 10).  The pages print no formula; the
+ * reading implemented here replaces GDN's scalar decay by a diagonal one over the
+ * key channels, applied before the delta rule reads the state.  Per (sequence,
+ * v head), tokens in order, with h = S^T [dk][dv]:
+ *
+ *   h_t = (I - beta_t k_t k_t^T) diag(exp g_t) h_{t-1} + beta_t k_t v_t^T,
+ *   o_t = h_t^T (scale q_t),                      g_t in R^dk, g_t <= 0.
+ *
+ * Arguments, layouts, ownership, streams and errors are those of gdn_chunk_fwd
+ * (bf16 q, k, v, o; fp32 state; GQA; cu_seqlens), except:
+ *   g     [B, T, Hv, dk] fp32, one log-decay per key channel, 16-byte aligned;
+ *         exact to the tolerance for g >= -10 per token and channel (the chunk
+ *         grams split exp(G_i - G_j) around each 16-token block's middle token,
+ *         and a factor must stay a normal fp32 number)
+ *   dk    128 only (GDN_ERR_UNSUPPORTED otherwise); dv 64 or 128
+ * kda_chunk_fwd_ex takes a caller-owned device workspace of at least
+ * kda_chunk_fwd_workspace_size(...) bytes, 256-byte aligned (0 for rejected
+ * sizes); kda_chunk_fwd takes one from the stream-ordered pool.
+ * kda_recurrent_step: one decode token (g [N, Hv, dk]; dk 64 or 128), as
+ * gdn_recurrent_step otherwise.
+ */
+gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream);
+gdn_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream);
+size_t kda_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
+                                    int has_cu_seqlens);
+gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream);
+
+/*
  * gdn_device_status - waits for `stream`, then reads and clears the device
  * error word that bounded device-side waits set when they give up.  Returns
  * GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the stream itself failed.

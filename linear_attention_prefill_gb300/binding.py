@@ -41,6 +41,10 @@ SIGNATURES = {
     "ssd_chunk_fwd_f32": (_I, _FWD_ARGS),
     "ssd_recurrent_step": (_I, _STEP_ARGS),
     "ssd_recurrent_step_f32": (_I, _STEP_ARGS),
+    "kda_chunk_fwd": (_I, _FWD_ARGS),
+    "kda_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "kda_chunk_fwd_workspace_size": (_SZ, [_I] * 8),
+    "kda_recurrent_step": (_I, _STEP_ARGS),
     "gdn_device_status": (_I, [_P]),
     "gdn_selftest_expired_wait": (_I, [ctypes.c_longlong, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
@@ -159,6 +163,27 @@ def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
                       output_final_state, stream, workspace)
 
 
+def kda_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) -> int:
+    """Bytes of workspace the KDA forward needs (0 for rejected sizes)."""
+    return int(load_library().kda_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk,
+                                                           int(bool(varlen))))
+
+
+def kda_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
+                  scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
+                  stream=None, workspace=None):
+    """Chunked-prefill forward of Kimi Delta Attention (bf16, dk = 128); returns (o, hT).
+
+    h_t = (I - beta_t k_t k_t^T) diag(exp g_t) h_{t-1} + beta_t k_t v_t^T,
+    o_t = h_t^T (scale q_t).  As gdn_chunk_fwd, except g is [B, T, Hv, dk] fp32:
+    one log-decay per key channel.  Runs kda_chunk_fwd_ex with ``workspace`` or a
+    fresh one.  ``scale`` defaults to dk^-0.5.
+    """
+    return _chunk_fwd("kda", q, k, v, g, beta, h0, o, hT, chunk,
+                      k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
+                      output_final_state, stream, workspace)
+
+
 def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output_final_state,
                stream, workspace, prologue=None):
     lib = load_library()
@@ -173,8 +198,10 @@ def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output
     _need(q, "q", dt, dev)
     _need(k, "k", dt, dev, q.shape)
     _need(v, "v", dt, dev, (B, T, Hv, dv))
-    _need(g, "g", torch.float32, dev, (B, T, Hv))
+    _need(g, "g", torch.float32, dev, (B, T, Hv, dk) if op == "kda" else (B, T, Hv))
     _need(beta, "beta", torch.float32, dev, (B, T, Hv))
+    if op == "kda" and dt != torch.bfloat16:
+        raise TypeError("the KDA forward takes bf16 q, k, v")
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
         if B != 1:
@@ -207,7 +234,8 @@ def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output
     if dt == torch.float32:
         _check(getattr(lib, f"{op}_chunk_fwd_f32")(*args, _stream_handle(stream, dev)))
         return o, hT
-    need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk, cu_seqlens is not None)
+    size_fn = kda_chunk_fwd_workspace_size if op == "kda" else gdn_chunk_fwd_workspace_size
+    need = size_fn(N, T, Hqk, Hv, dk, dv, chunk, cu_seqlens is not None)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
@@ -238,6 +266,15 @@ def ssd_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: float = 1.0, strea
     return _step("ssd", q, k, v, g, beta, h, o, scale, stream)
 
 
+def kda_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = None,
+                       stream=None):
+    """One decode token of Kimi Delta Attention (g [N, Hv, dk]); updates h, returns o."""
+    if q.dtype != torch.bfloat16:
+        raise TypeError("the KDA decode step takes bf16 q, k, v")
+    return _step("kda", q, k, v, g, beta, h, o, k.shape[-1] ** -0.5 if scale is None else scale,
+                 stream)
+
+
 def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None):
     lib = load_library()
     dev = q.device
@@ -247,7 +284,7 @@ def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None):
     _need(q, "q", dt, dev)
     _need(k, "k", dt, dev, q.shape)
     _need(v, "v", dt, dev, (N, Hv, dv))
-    _need(g, "g", torch.float32, dev, (N, Hv))
+    _need(g, "g", torch.float32, dev, (N, Hv, dk) if op == "kda" else (N, Hv))
     _need(beta, "beta", torch.float32, dev, (N, Hv))
     _need(h, "h", torch.float32, dev, (N, Hv, dk, dv))
     if o is None:
@@ -284,7 +321,7 @@ def gdn_device_status(stream=None):
 def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None,
                        op: str = "gdn"):
     """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out
-    (``op`` "ssd" runs ssd_chunk_fwd instead).
+    (``op`` "ssd" runs ssd_chunk_fwd, "kda" kda_chunk_fwd instead).
 
     ``inputs`` holds pinned CPU tensors q, k, v, g, beta and optionally h0 and
     cu_seqlens.  ``out`` may hold preallocated pinned (o, hT) host tensors and
@@ -305,13 +342,13 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         buf.copy_(t, non_blocking=True)
         d[name] = buf
         nbytes_in += t.numel() * t.element_size()
-    fwd = ssd_chunk_fwd if op == "ssd" else gdn_chunk_fwd
+    fwd = {"ssd": ssd_chunk_fwd, "kda": kda_chunk_fwd}.get(op, gdn_chunk_fwd)
     if "workspace" not in bufs:
         B, T, Hqk, dk = d["q"].shape
         Hv, dv = d["v"].shape[2], d["v"].shape[3]
         N = d["cu_seqlens"].numel() - 1 if d["cu_seqlens"] is not None else B
-        need = gdn_chunk_fwd_workspace_size(N, T, Hqk, Hv, dk, dv, chunk,
-                                            d["cu_seqlens"] is not None)
+        size_fn = kda_chunk_fwd_workspace_size if op == "kda" else gdn_chunk_fwd_workspace_size
+        need = size_fn(N, T, Hqk, Hv, dk, dv, chunk, d["cu_seqlens"] is not None)
         bufs["workspace"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     o_dev, hT_dev = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], bufs.get("o"),
                         bufs.get("hT"), chunk=chunk, cu_seqlens=d["cu_seqlens"], stream=stream,

@@ -115,6 +115,7 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   p->prologue = 0;
   p->A_log = nullptr;
   p->dt_bias = nullptr;
+  p->kda = 0;
   return GDN_OK;
 }
 
@@ -151,6 +152,22 @@ gdn_status check_step(const void* q, const void* k, const void* v, const float* 
   p->prologue = 0;
   p->A_log = nullptr;
   p->dt_bias = nullptr;
+  p->kda = 0;
+  return GDN_OK;
+}
+
+// Kimi Delta Attention: the forward's checks plus dk = 128 and a 16-byte aligned
+// per-channel gate g [B, T, Hv, dk].
+gdn_status check_kda(const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                     int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                     const int32_t* cu_seqlens, gdn::FwdParams* p) {
+  gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, 2, p);
+  if (s != GDN_OK) return s;
+  if (dk != 128) return fail(GDN_ERR_UNSUPPORTED, "dk=%d: the KDA forward takes dk = 128", dk);
+  if (!aligned(g, 16)) return fail(GDN_ERR_INVALID_ARG, "g must be 16-byte aligned for KDA");
+  p->kda = 1;
   return GDN_OK;
 }
 
@@ -184,7 +201,7 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
 }
 
 gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
-  cudaError_t e = gdn::launch_prep(p, w, stream);
+  cudaError_t e = p.kda ? gdn::launch_kda_prep(p, w, stream) : gdn::launch_prep(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
   if (w.blocks) {  // dk = dv = 128, gated delta rule: 128-token blocks
     if (gdn::scan_out_fused(p)) {  // pair, scan and output work in one launch
@@ -401,6 +418,52 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
   if (s != GDN_OK) return s;
   p.delta_rule = 0;
   return run_step(p, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- Kimi Delta Attention: the delta rule with a per-channel gate ------------------
+gdn_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                            int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
+                            gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_kda(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* h0, void* o, float* hT, int B, int T,
+                         int Hqk, int Hv, int dk, int dv, int chunk, float scale,
+                         const int32_t* cu_seqlens, gdn_stream_t stream) {
+  gdn::FwdParams p;
+  gdn_status s = check_kda(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
+                           cu_seqlens, &p);
+  if (s != GDN_OK) return s;
+  return fwd_bf16_pooled(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kda_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
+                                    int has_cu_seqlens) {
+  gdn::FwdParams p;
+  static const int32_t fake_cu = 0;
+  const void* A = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  if (check_kda(A, A, A, static_cast<const float*>(A), static_cast<const float*>(A), nullptr,
+                const_cast<void*>(A), nullptr, B, T, Hqk, Hv, dk, dv, chunk, 1.0f,
+                has_cu_seqlens ? &fake_cu : nullptr, &p) != GDN_OK)
+    return 0;
+  return gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+}
+
+gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                              int dk, int dv, float scale, gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  p.kda = 1;
+  return run_step(p, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_selftest_expired_wait(long long limit_cycles, gdn_stream_t stream) {

@@ -23,6 +23,12 @@
 // Precision: every product takes fp16 operands with fp32 accumulation; the
 // output warps scale their bf16 q fragments by scale gamma_i and round them to
 // fp16 in registers, so q needs no converted copy anywhere.
+//
+// KDA mode (Kimi Delta Attention, the per-channel gate; records from
+// kda_prep.cu): the decay of the state update is one factor per state row,
+// h <- diag(exp G_last) h + Kt^T V_new, and the output's left factor
+// Q~ = scale Q * exp(G) varies per channel, so the producer stages the fp16 Q~
+// record instead of q and the output warps use it as it is.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -72,7 +78,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t x, float s) 
   return pack_f16(f.x * s, f.y * s);
 }
 
-template <int DK, int DVT>
+template <int DK, int DVT, bool KDA>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chain_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq) {
   using Lo = ChainLayout<DK, DVT>;
@@ -155,10 +161,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_g2s(st + Lo::kP, ws.P(slot, hv, p.Hv), kC * kC * 2, bar);
         bulk_g2s(st + Lo::kUt, ws.U(slot, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
         bulk_g2s(st + Lo::kGv, ws.gv(slot, hv, p.Hv), kGvFloats * 4, bar);
-        const int row = (int)(t_seq + (long long)c * kC);
+        if constexpr (KDA) {  // Q~, already in the q tile's layout
+          bulk_g2s(st + Lo::kQ, ws.Qt(slot, hv, p.Hv), kC * DK * 2, bar);
+        } else {
+          const int row = (int)(t_seq + (long long)c * kC);
 #pragma unroll
-        for (int kb = 0; kb < DK / 64; ++kb)
-          tma_load_2d(st + Lo::kQ + kb * 8192, &tmq, hq * DK + kb * 64, row, bar);
+          for (int kb = 0; kb < DK / 64; ++kb)
+            tma_load_2d(st + Lo::kQ + kb * 8192, &tmq, hq * DK + kb * 64, row, bar);
+        }
       };
       for (int c = 0; c < kStages && c < n_chunks; ++c) issue(c);
       for (int c = 0; c + kStages < n_chunks; ++c) {
@@ -198,10 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ks < DK / 16; ++ks) {
         uint32_t a[4];
         load_a_sw128(a, st + Lo::kQ, m0, 16 * ks, lane);
-        a[0] = bf16x2_to_f16x2_scaled(a[0], s0);
-        a[1] = bf16x2_to_f16x2_scaled(a[1], s1);
-        a[2] = bf16x2_to_f16x2_scaled(a[2], s0);
-        a[3] = bf16x2_to_f16x2_scaled(a[3], s1);
+        if constexpr (!KDA) {
+          a[0] = bf16x2_to_f16x2_scaled(a[0], s0);
+          a[1] = bf16x2_to_f16x2_scaled(a[1], s1);
+          a[2] = bf16x2_to_f16x2_scaled(a[2], s0);
+          a[3] = bf16x2_to_f16x2_scaled(a[3], s1);
+        }
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
           uint32_t bb[4];
@@ -318,14 +330,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) mbar_arrive(&pub[hb]);
 
     // #5 update: h = gamma_last h + Kt^T V_new, written straight into H[hn]
+    // (KDA: row r of h decays by exp(G_last) of key channel r)
     {
-      const float gl = reinterpret_cast<const float*>(st + Lo::kGv)[0];
+      const float* gvs = reinterpret_cast<const float*>(st + Lo::kGv);
 #pragma unroll
-      for (int mt = 0; mt < MTW; ++mt)
+      for (int mt = 0; mt < MTW; ++mt) {
+        const int hr = 16 * (MTW * warp + mt) + gq;
+        const float g0 = KDA ? gvs[4 + hr] : gvs[0], g1 = KDA ? gvs[4 + hr + 8] : gvs[0];
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int x = 0; x < 4; ++x) hacc[mt][j][x] *= gl;
+        for (int j = 0; j < NT; ++j) {
+          hacc[mt][j][0] *= g0;
+          hacc[mt][j][1] *= g0;
+          hacc[mt][j][2] *= g1;
+          hacc[mt][j][3] *= g1;
+        }
+      }
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
 #pragma unroll
@@ -383,11 +402,21 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
   const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
   CUtensorMap mq;
   if (!make_tensor_map_bf16(&mq, p.q, rows, (long long)p.Hqk * DK)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT>,
+  const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
+  if (p.kda) {  // KDA records exist for dk = 128 only
+    if constexpr (DK == 128) {
+      cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
+      if (e != cudaSuccess) return e;
+      gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
+      return cudaGetLastError();
+    }
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
-  gdn_chain_kernel<DK, DVT><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
+  gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
   return cudaGetLastError();
 }
 

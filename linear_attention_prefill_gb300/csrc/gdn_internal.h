@@ -32,6 +32,9 @@ struct FwdParams {
   int prologue;
   const float* A_log;
   const float* dt_bias;
+  // Kimi Delta Attention (kda != 0, dk = 128): g is [B, T, Hv, dk], one log-decay per
+  // key channel; h_t = (I - beta k k^T) diag(exp g_t) h_{t-1} + beta k v^T.
+  int kda;
 };
 constexpr float kNormEps = 1e-6f;
 
@@ -50,6 +53,7 @@ struct StepParams {
   int prologue;       // as in FwdParams: raw q, k, gates a (in g) and b (in beta)
   const float* A_log;
   const float* dt_bias;
+  int kda;            // 1: g is [N, Hv, dk], a per-channel decay of the state rows
 };
 
 // Workspace of the bf16 forward: one record per (chunk slot, v head), written
@@ -64,6 +68,11 @@ struct StepParams {
 //                   tile j is the contiguous rows [j t, (j + 1) t)
 //   gv   fp32 [132] gamma_last, 3 pad, gamma_i = exp(G_i) for the 64 rows, then
 //                   e_j for the 64 rows (norm factors folded in with the prologue)
+// Kimi Delta Attention records (kda_prep.cu, dk = 128) are the same tiles with
+// the per-channel gate inside (W = Tm diag(beta) (K * exp G), Kt = K *
+// exp(G_last - G), P with exp(G_i - G_j) inside the channel sum), gv[4 + c] =
+// exp(G_last,c) for the 128 key channels, and one more tile:
+//   Qt   [64][dk]   scale Q * exp(G), swzb<64>, fp16 (the output's left factor)
 // Every 16-bit tile is in the tensor cores' 128-byte-swizzled layout, so the
 // same bytes serve ldmatrix loads and tcgen05 operand descriptors.
 // The dv tile t (16 or 32 columns, one chain CTA each) is picked per call by
@@ -93,7 +102,7 @@ struct WsLayout {
   int dvt;                  // dv tile width of the chain launch
   long long n_slots;        // chunk slots per v head
   long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
-  long long task_bytes, kt_off, p_off, u_off, gv_off;
+  long long task_bytes, kt_off, p_off, u_off, gv_off, qt_off;
   int blocks;               // 1: the block path runs (pair records present)
   long long n_bslots, bslots_per_seq, pair_off, pair_bytes, pb_off, ph_off, pg_off;
   // fused scan launch: [n_bslots][Hv] pair-done flags, [n_bslots][Hv][2]
@@ -147,6 +156,9 @@ struct WsLayout {
   __host__ __device__ float* gv(long long s, int hv, int Hv) const {
     return reinterpret_cast<float*>(rec(s, hv, Hv) + gv_off);
   }
+  __host__ __device__ __half* Qt(long long s, int hv, int Hv) const {
+    return reinterpret_cast<__half*>(rec(s, hv, Hv) + qt_off);
+  }
   __device__ long long first_slot(const FwdParams& p, int n) const {
     if (p.cu_seqlens) return (long long)(p.cu_seqlens[n] / kChunk) + n;
     return (long long)n * slots_per_seq;
@@ -182,8 +194,10 @@ inline WsLayout ws_layout(const FwdParams& p, void* base) {
   w.p_off = 2 * wk;
   w.u_off = w.p_off + (long long)kChunk * kChunk * 2;
   w.gv_off = w.u_off + wv;
-  w.task_bytes = (w.gv_off + kGvFloats * 4 + 127) / 128 * 128;  // records on 128-byte lines
-  w.blocks = p.delta_rule && p.dk == 128 && p.dv == 128 && block_path_enabled();
+  w.qt_off = (w.gv_off + kGvFloats * 4 + 127) / 128 * 128;
+  // records on 128-byte lines; the KDA record adds the Qt tile
+  w.task_bytes = p.kda ? (w.qt_off + wk + 127) / 128 * 128 : w.qt_off;
+  w.blocks = !p.kda && p.delta_rule && p.dk == 128 && p.dv == 128 && block_path_enabled();
   if (p.cu_seqlens) {
     w.bslots_per_seq = 0;
     w.n_bslots = (long long)p.T / kBlock + p.N + 1;
@@ -257,6 +271,8 @@ bool make_tensor_map_bf16_3d(CUtensorMap* m, const void* base, long long planes,
 
 // Launchers: return cudaSuccess or the launch error.  Each validates nothing.
 cudaError_t launch_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
+// Kimi Delta Attention records (kda_prep.cu; p.kda, dk = 128).
+cudaError_t launch_kda_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_chain(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 // The block path (ws.blocks): pair transitions, the block scan, the block output.
 cudaError_t launch_pair(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);

@@ -7,7 +7,8 @@
 // Per token, with h = S^T of shape [dk, dv]:
 //   h <- exp(g) h;  u = beta (v - h^T k);  h <- h + k u^T;  o = h^T (scale q)
 // and, without the erase term (the Mamba-2 SSD recurrence of "Exp 2026-07-13 —
-// Linear-Attention Scans on the NPU", §1 and §3), u = beta v.
+// Linear-Attention Scans on the NPU", §1 and §3), u = beta v.  For Kimi Delta
+// Attention the decay is per key channel: h <- diag(exp g) h with g [dk].
 // The state is read once and written once, so the step is bound by HBM
 // bandwidth: each CTA streams a [dk, 32] column tile of h with 128-byte
 // coalesced rows, keeps it in registers between the two column reductions.
@@ -27,7 +28,7 @@ __device__ __forceinline__ void store(__nv_bfloat16* p, float x) { *p = __float2
 
 template <typename TIn, int DK>
 __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams p) {
-  __shared__ float sk[DK], sq[DK];
+  __shared__ float sk[DK], sq[DK], sa[DK];  // sa: KDA's per-channel decay
   __shared__ float red1[kWarps][kCols], red2[kWarps][kCols];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntile = p.dv / kCols;
@@ -70,13 +71,15 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
     sq[i] *= rq * p.scale;
   }
   const long long nh = (long long)n * p.Hv + hv;
-  float gate = p.g[nh], b = p.beta[nh];
+  float gate = p.kda ? 0.f : p.g[nh], b = p.beta[nh];
   if (p.prologue) {  // raw gates: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
     const float x = gate + (p.dt_bias ? p.dt_bias[hv] : 0.f);
     gate = -(p.A_log ? expf(p.A_log[hv]) : 1.f) * (x > 20.f ? x : log1pf(expf(x)));
     b = 1.f / (1.f + expf(-b));
   }
-  const float alpha = expf(gate);
+  const float alpha = p.kda ? 0.f : expf(gate);
+  if (p.kda)  // Kimi Delta Attention: row r of h decays by exp(g[r])
+    for (int i = tid; i < DK; i += kWarps * 32) sa[i] = expf(p.g[nh * DK + i]);
   const int col = tile * kCols + lane;
   const float vcol = to_f(static_cast<const TIn*>(p.v)[nh * p.dv + col]);
   __syncthreads();
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = warp + kWarps * i;
-    hr[i] = alpha * h[(long long)r * p.dv];
+    hr[i] = (p.kda ? sa[r] : alpha) * h[(long long)r * p.dv];
     part += hr[i] * sk[r];
   }
   red1[warp][lane] = part;

@@ -1,0 +1,385 @@
+// kda_prep.cu - the chunk-parallel Map phase of Kimi Delta Attention (KDA).
+//
+// KDA is the delta rule with a per-key-channel gate ("Empowering Hybrid
+// Attention Models on NPUs": GDN and KDA share the Map-Reduce-Map paradigm of
+// §2.1, Figure 1(b); KDA's gate is one fp32 value per token, head and channel,
+// Figure 4(a)).  Per (sequence, v head), with the state h = S^T [dk][dv]:
+//   h_t = (I - beta_t k_t k_t^T) diag(exp g_t) h_{t-1} + beta_t k_t v_t^T,
+//   o_t = h_t^T (scale q_t).
+// Per chunk (local i, j; G = the per-channel cumulative gate):
+//   #1 Gate   G_i = sum_{s<=i} g_s                       [64][dk]
+//   #2 KKT    A_ij = beta_i sum_c k_ic k_jc exp(G_ic - G_jc)   (j < i)
+//      QK^T   P_ij = scale sum_c q_ic k_jc exp(G_ic - G_jc)    (j <= i)
+//   #3 Solve  Tm = (I + A)^-1
+//   #4 W/U    W = Tm diag(beta) (K * exp G),  U = Tm diag(beta) V
+// plus Kt = K * exp(G_last - G) (the state update's left factor), the output's
+// Q~ = scale Q * exp(G) and the per-channel carry exp(G_last).  The chain
+// (gdn_chain.cu, KDA mode) reads this record exactly as the GDN one, with Q~ in
+// place of q and a per-row state decay.
+//
+// The grams.  exp(G_ic - G_jc) differs per channel, so it cannot leave the
+// channel sum as GDN's scalar mask does; it is split around a reference token s
+// per 16-row block I of the chunk (s = 16 I + 7, the block's middle):
+//   A_ij = beta_i sum_c [k_ic exp(G_ic - G_sc)] [k_jc exp(G_sc - G_jc)],
+// one tf32 tensor-core product per block row.  For j < 16 I the right factor
+// is at most 1; within the block both factors stay within exp(8 max|g|), so
+// every factor is a normal fp32 number for log-decays down to about -10 per
+// token and channel (the input recipe draws g = -softplus(N(mu, 1)) s), and a
+// factor that underflows multiplies a product that is itself below 1e-30.
+// Everything else takes exp of differences that are <= 0.
+//
+// Layout and work: one CTA of 256 threads per (chunk slot, v head), ~106 KB of
+// shared memory (two CTAs per SM); loads by cp.async (rows past the sequence
+// zero-filled), the grams on tf32 mma.sync, the solve in fp32 on the CUDA
+// cores (gdn_common.cuh), W^T and U^T on fp16 mma.sync.  No waits other than
+// cp.async groups and CTA barriers.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kC = 64;
+constexpr int kThreads = 256;
+constexpr int kDK = 128;  // key head dim: the gate's channels
+constexpr int kLd = 68;   // fp32 operand row stride: conflict-free tf32 fragment loads
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared-memory map (byte offsets from a 128-aligned base).
+template <int DV>
+struct KdaLayout {
+  static constexpr int kK = 0;                  // bf16 [64][128] swz<128>; later K~ fp16
+  static constexpr int kQ = kK + kC * kDK * 2;  // bf16 [64][128] swz<128>; later Tb fp16 [64][64] swz<64>
+  static constexpr int kG = kQ + kC * kDK * 2;  // fp32 [64][128] G; later T fp32 [64][64], X [768]
+  static constexpr int kA = kG + kC * kDK * 4;  // fp32 [64][64] A (strictly lower part)
+  static constexpr int kS = kA + kC * kC * 4;   // RK, RQ [16][kLd], C [64][kLd] fp32; later V
+  static constexpr int kSBytes = (16 + 16 + 64) * kLd * 4;
+  static constexpr int kVec = kS + kSBytes;     // beta [64], column totals [128]
+  static constexpr int kBytes = kVec + (kC + kDK) * 4;
+  static constexpr int kAlloc = kBytes + 128;   // slack to align the base
+  static_assert(kC * DV * 2 <= kSBytes, "V fits the scratch");
+  static_assert(kC * kC * 4 + 3 * 256 * 4 <= kC * kDK * 4, "T and X fit G's space");
+};
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// D = A * B + D for one m16n8k8 step, tf32 inputs, fp32 accumulation.  Fragments:
+// a0 (row gq, k tq), a1 (gq + 8, tq), a2 (gq, tq + 4), a3 (gq + 8, tq + 4);
+// b0 (k tq, col gq), b1 (k tq + 4, col gq); d as for m16n8k16.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two B fragments (k16 x n8, n tiles n0 and n0 + 8) of a tile stored as [n][k]
+// in the swizzled layout swz<W>.
+template <int W>
+__device__ __forceinline__ void load_b_nk_sw(uint32_t (&b)[4], const __half* base, int n0, int k0,
+                                             int lane) {
+  const int g = lane >> 3;
+  ldsm_x4(b[0], b[1], b[2], b[3],
+          base + swz<W>(n0 + (lane & 7) + ((g >> 1) << 3), k0 + ((g & 1) << 3)));
+}
+__device__ __forceinline__ void unpack_bf16x8(const void* p, float (&f)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(b[i]);
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8_f16(const float (&x)[8]) {
+  return make_uint4(pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]),
+                    pack_f16(x[6], x[7]));
+}
+__device__ __forceinline__ float exp_of(float x) { return ex2_approx(x * kLog2e); }
+
+template <int DV>
+__global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p, const WsLayout ws) {
+  using Lo = KdaLayout<DV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + Lo::kK);
+  __half* Kh = reinterpret_cast<__half*>(sm + Lo::kK);   // K~ after the grams
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + Lo::kQ);
+  __half* Tb = reinterpret_cast<__half*>(sm + Lo::kQ);   // Tm diag(beta) after the grams
+  float* Gs = reinterpret_cast<float*>(sm + Lo::kG);
+  float* Ts = Gs;                                        // Tm after the grams
+  float* Xs = Gs + kC * kC;
+  float* As = reinterpret_cast<float*>(sm + Lo::kA);
+  float* RK = reinterpret_cast<float*>(sm + Lo::kS);
+  float* RQ = RK + 16 * kLd;
+  float* Cm = RQ + 16 * kLd;
+  __half* Vh = reinterpret_cast<__half*>(sm + Lo::kS);   // V after the grams
+  float* s_beta = reinterpret_cast<float*>(sm + Lo::kVec);
+  float* s_tot = s_beta + kC;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int hv = blockIdx.x % p.Hv;
+  const long long slot = blockIdx.x / p.Hv;
+  int n, c;
+  if (!locate_chunk(p, ws, slot, &n, &c)) return;
+  const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
+  const long long len =
+      p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
+  const long long t0 = t_seq + (long long)c * kC;  // first token of the chunk
+  const int L = (int)min((long long)kC, len - (long long)c * kC);
+  const int hq = hv / (p.Hv / p.Hqk);
+  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k);
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
+  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v);
+
+  // ---- loads: K, Q (bf16) and g (fp32 per channel); rows past the sequence are zero
+  for (int i = tid; i < kC * (kDK / 8); i += kThreads) {
+    const int r = i / (kDK / 8), ch = i % (kDK / 8);
+    const bool ok = r < L;
+    const long long off = ((ok ? t0 + r : t0) * p.Hqk + hq) * kDK + ch * 8;
+    cp_async16(Ks + swz<kDK>(r, ch * 8), kg + off, ok);
+    cp_async16(Qs + swz<kDK>(r, ch * 8), qg + off, ok);
+  }
+  for (int i = tid; i < kC * (kDK / 4); i += kThreads) {
+    const int r = i / (kDK / 4), ch = i % (kDK / 4);
+    const bool ok = r < L;
+    cp_async16(Gs + r * kDK + ch * 4, p.g + ((ok ? t0 + r : t0) * p.Hv + hv) * kDK + ch * 4, ok);
+  }
+  cp_async_commit();
+  if (tid < kC) s_beta[tid] = tid < L ? p.beta[(t0 + tid) * p.Hv + hv] : 0.f;
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- #1 Gate: per-channel inclusive cumsum over the chunk (two threads a channel)
+  {
+    const int ch = tid % kDK, half = tid / kDK;
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = Gs[(32 * half + i) * kDK + ch];
+#pragma unroll
+    for (int i = 1; i < 32; ++i) x[i] += x[i - 1];
+    if (half == 0) s_tot[ch] = x[31];
+    __syncthreads();
+    const float base = half ? s_tot[ch] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) Gs[(32 * half + i) * kDK + ch] = x[i] + base;
+  }
+  __syncthreads();
+  const float* GL = Gs + (kC - 1) * kDK;  // G of the last row = G_last (rows past L add 0)
+  {
+    float* gv = ws.gv(slot, hv, p.Hv);  // [0..3] unused, [4 + c] = exp(G_last,c)
+    if (tid < kDK) gv[4 + tid] = expf(GL[tid]);
+    if (tid < 4) gv[tid] = 0.f;
+  }
+
+  // ---- Kt = K * exp(G_last - G) and Q~ = scale Q * exp(G) (fp16 records) -----------
+  {
+    __half* Kt = ws.Kt(slot, hv, p.Hv);
+    __half* Qt = ws.Qt(slot, hv, p.Hv);
+    for (int i = tid; i < kC * (kDK / 8); i += kThreads) {
+      const int r = i / (kDK / 8), ch = i % (kDK / 8);
+      float kf[8], qf[8], kt[8], qt[8];
+      unpack_bf16x8(Ks + swz<kDK>(r, ch * 8), kf);
+      unpack_bf16x8(Qs + swz<kDK>(r, ch * 8), qf);
+      const float* Gr = Gs + r * kDK + ch * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        kt[e] = kf[e] * exp_of(GL[ch * 8 + e] - Gr[e]);
+        qt[e] = p.scale * qf[e] * exp_of(Gr[e]);
+      }
+      *reinterpret_cast<uint4*>(Kt + swzb<kC>(r, ch * 8)) = pack8_f16(kt);
+      *reinterpret_cast<uint4*>(Qt + swzb<kC>(r, ch * 8)) = pack8_f16(qt);
+    }
+  }
+
+  // ---- #2 grams, one 16-row block row I at a time, channels in two halves ----------
+  __half* Pg = ws.P(slot, hv, p.Hv);
+  for (int I = 0; I < 4; ++I) {
+    const int nc = 16 * (I + 1);  // columns 0 .. nc - 1
+    const int nt = nc / 8;        // n8 tiles of each gram
+    const int jobs = 2 * nt;      // A tiles, then P tiles: at most two per warp
+    const int s = 16 * I + 7;     // reference token of the block row
+    float acc[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[u][x] = 0.f;
+    for (int hf = 0; hf < 2; ++hf) {
+      const int c0 = 64 * hf;
+      __syncthreads();  // the scratch is free
+      const float* Gref = Gs + s * kDK + c0;
+      for (int e = tid; e < 16 * 64; e += kThreads) {
+        const int i = e >> 6, cc = e & 63, j = 16 * I + i;
+        const float f = exp_of(Gs[j * kDK + c0 + cc] - Gref[cc]);
+        RK[i * kLd + cc] = __bfloat162float(Ks[swz<kDK>(j, c0 + cc)]) * f;
+        RQ[i * kLd + cc] = __bfloat162float(Qs[swz<kDK>(j, c0 + cc)]) * f;
+      }
+      for (int e = tid; e < nc * 64; e += kThreads) {
+        const int m = e >> 6, cc = e & 63;
+        Cm[m * kLd + cc] =
+            __bfloat162float(Ks[swz<kDK>(m, c0 + cc)]) * exp_of(Gref[cc] - Gs[m * kDK + c0 + cc]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int jb = warp + 8 * u;
+        if (jb < jobs) {
+          const bool isP = jb >= nt;
+          const int n0 = 8 * (isP ? jb - nt : jb);
+          const float* R = isP ? RQ : RK;
+#pragma unroll
+          for (int k0 = 0; k0 < 64; k0 += 8) {
+            uint32_t a[4];
+            a[0] = to_tf32(R[gq * kLd + k0 + tq]);
+            a[1] = to_tf32(R[(gq + 8) * kLd + k0 + tq]);
+            a[2] = to_tf32(R[gq * kLd + k0 + tq + 4]);
+            a[3] = to_tf32(R[(gq + 8) * kLd + k0 + tq + 4]);
+            mma_tf32(acc[u], a, to_tf32(Cm[(n0 + gq) * kLd + k0 + tq]),
+                     to_tf32(Cm[(n0 + gq) * kLd + k0 + tq + 4]));
+          }
+        }
+      }
+    }
+    // block row I of A (fp32, shared) and P (fp16 record), masked to the triangles
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int jb = warp + 8 * u;
+      if (jb < jobs) {
+        const bool isP = jb >= nt;
+        const int n0 = 8 * (isP ? jb - nt : jb);
+#pragma unroll
+        for (int xh = 0; xh < 2; ++xh) {
+          const int i = 16 * I + gq + 8 * xh, m = n0 + 2 * tq;
+          const float v0 = acc[u][2 * xh], v1 = acc[u][2 * xh + 1];
+          if (isP) {
+            *reinterpret_cast<uint32_t*>(Pg + swz<kC>(i, m)) =
+                pack_f16(m <= i ? p.scale * v0 : 0.f, m + 1 <= i ? p.scale * v1 : 0.f);
+          } else {
+            As[i * kC + m] = m < i ? s_beta[i] * v0 : 0.f;
+            As[i * kC + m + 1] = m + 1 < i ? s_beta[i] * v1 : 0.f;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();  // grams done: the Q rows, the scratch and (after K~) G are free
+
+  // ---- K~ = K * exp(G) in place (fp16), V into the scratch -------------------------
+  for (int i = tid; i < kC * (kDK / 8); i += kThreads) {
+    const int r = i / (kDK / 8), ch = i % (kDK / 8);
+    float f[8];
+    unpack_bf16x8(Ks + swz<kDK>(r, ch * 8), f);
+    const float* Gr = Gs + r * kDK + ch * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] *= exp_of(Gr[e]);
+    *reinterpret_cast<uint4*>(Kh + swz<kDK>(r, ch * 8)) = pack8_f16(f);
+  }
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {
+    const int r = i / (DV / 8), ch = i % (DV / 8);
+    const bool ok = r < L;
+    cp_async16(Vh + swz<DV>(r, ch * 8), vg + ((ok ? t0 + r : t0) * p.Hv + hv) * DV + ch * 8, ok);
+  }
+  cp_async_commit();
+  __syncthreads();  // G is dead: its space takes Tm
+
+  // ---- #3 Solve: Tm = (I + A)^-1 in fp32; then Tb = Tm diag(beta) in fp16 -----------
+  solve_unit_lower_64_f32<kThreads>(As, kC, Ts, kC, Xs);  // ends with a barrier
+  for (int i = tid; i < kC * 8; i += kThreads) {
+    const int r = i >> 3, ch = i & 7;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = Ts[r * kC + ch * 8 + e] * s_beta[ch * 8 + e];
+    *reinterpret_cast<uint4*>(Tb + swz<kC>(r, ch * 8)) = pack8_f16(x);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  for (int i = tid; i < kC * (DV / 8); i += kThreads) {
+    const int r = i / (DV / 8), ch = i % (DV / 8);
+    bf16x8_to_f16x8(Vh + swz<DV>(r, ch * 8));
+  }
+  __syncthreads();
+
+  // ---- #4 W^T = K~^T Tb^T and U^T = V^T Tb^T (fp16 mma.sync; one d row block a warp)
+  {
+    __half* Wt = ws.W(slot, hv, p.Hv);  // [dk][64], swz<64>
+    const int m0 = 16 * warp;
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[j][x] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks) {
+      uint32_t a[4];
+      load_a_trans_sw<kDK>(a, Kh, m0, 16 * ks, lane);
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        uint32_t b[4];
+        load_b_nk_sw<kC>(b, Tb, 8 * j, 16 * ks, lane);
+        mma_f16(acc[j], a, b[0], b[1]);
+        mma_f16(acc[j + 1], a, b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int col = 8 * j + 2 * tq;
+      *reinterpret_cast<uint32_t*>(Wt + swz<kC>(m0 + gq, col)) = pack_f16(acc[j][0], acc[j][1]);
+      *reinterpret_cast<uint32_t*>(Wt + swz<kC>(m0 + gq + 8, col)) = pack_f16(acc[j][2], acc[j][3]);
+    }
+  }
+  if (warp < DV / 16) {
+    __half* Ut = ws.U(slot, hv, p.Hv);  // [dv][64], swz<64>
+    const int m0 = 16 * warp;
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) acc[j][x] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kC / 16; ++ks) {
+      uint32_t a[4];
+      load_a_trans_sw<DV>(a, Vh, m0, 16 * ks, lane);
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        uint32_t b[4];
+        load_b_nk_sw<kC>(b, Tb, 8 * j, 16 * ks, lane);
+        mma_f16(acc[j], a, b[0], b[1]);
+        mma_f16(acc[j + 1], a, b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int col = 8 * j + 2 * tq;
+      *reinterpret_cast<uint32_t*>(Ut + swz<kC>(m0 + gq, col)) = pack_f16(acc[j][0], acc[j][1]);
+      *reinterpret_cast<uint32_t*>(Ut + swz<kC>(m0 + gq + 8, col)) = pack_f16(acc[j][2], acc[j][3]);
+    }
+  }
+}
+
+template <int DV>
+cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  using Lo = KdaLayout<DV>;
+  cudaError_t e = cudaFuncSetAttribute(kda_prep_kernel<DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
+  if (e != cudaSuccess) return e;
+  const long long grid = ws.n_slots * p.Hv;
+  kda_prep_kernel<DV><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kda_prep(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
+  if (p.dk != kDK) return cudaErrorInvalidValue;
+  return p.dv == 128 ? launch_t<128>(p, ws, stream) : launch_t<64>(p, ws, stream);
+}
+
+}  // namespace gdn

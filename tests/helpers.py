@@ -3,7 +3,7 @@ very tensors handed to the kernel, and the error measure of the tolerance."""
 import numpy as np
 import torch
 
-from oracle import gdn_recurrent, qk_head, ssd_recurrent
+from oracle import gdn_recurrent, kda_recurrent, qk_head, ssd_recurrent
 
 # max |x - x_ref| / RMS(x_ref): bf16 inputs with fp32 accumulation, and the fp32 path.
 # o is stored in the input dtype; for bf16 the comparison first allows the half-ulp
@@ -70,7 +70,7 @@ def oracle_heads(x, heads, seqs=None, op="gdn"):
             hq = qk_head(hv, Hqk, Hv)
             sl = slice(t0, t1)
             h0n = None if h0 is None else to_np(h0[n:n + 1, hv:hv + 1])
-            fwd = gdn_recurrent if op == "gdn" else ssd_recurrent
+            fwd = {"gdn": gdn_recurrent, "ssd": ssd_recurrent, "kda": kda_recurrent}[op]
             o, hT = fwd(to_np(q[b:b + 1, sl, hq:hq + 1]), to_np(k[b:b + 1, sl, hq:hq + 1]),
                                   to_np(v[b:b + 1, sl, hv:hv + 1]), to_np(g[b:b + 1, sl, hv:hv + 1]),
                                   to_np(beta[b:b + 1, sl, hv:hv + 1]), x["scale"], h0n)
@@ -79,7 +79,7 @@ def oracle_heads(x, heads, seqs=None, op="gdn"):
 
 
 def check_heads(x, o, hT, heads, dtype, seqs=None, tol=None, op="gdn"):
-    """Compare the kernel's o / hT with the oracle (``op`` "gdn" or "ssd") on the chosen
+    """Compare the kernel's o / hT with the oracle (``op`` "gdn", "ssd" or "kda") on the chosen
     chains; returns the worst errors."""
     tol = TOL[dtype] if tol is None else tol
     ref = oracle_heads(x, heads, seqs, op)

@@ -20,7 +20,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gdn|ssd)_\w+)\s*\(", text,
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gdn|ssd|kda)_\w+)\s*\(", text,
                                  flags=re.M)))
 
 
@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
                  "gdn_device_status", "gdn_abi_version", "ssd_chunk_fwd", "ssd_chunk_fwd_ex",
                  "ssd_chunk_fwd_f32", "ssd_recurrent_step", "ssd_recurrent_step_f32",
                  "gdn_chunk_fwd_prologue", "gdn_chunk_fwd_prologue_ex",
-                 "gdn_recurrent_step_prologue", "gdn_selftest_expired_wait"):
+                 "gdn_recurrent_step_prologue", "gdn_selftest_expired_wait", "kda_chunk_fwd",
+                 "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size", "kda_recurrent_step"):
         assert want in names
 
 
@@ -156,3 +157,34 @@ def test_ex_rejects_small_or_misaligned_workspace(lib):
     assert lib.gdn_chunk_fwd_ex(*args, A, need - 1, None) == 1
     assert lib.gdn_chunk_fwd_ex(*args, A + 16, need, None) == 1
     assert b"workspace" in lib.gdn_last_error()
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(q=None), 1), (dict(g=None), 1), (dict(Hqk=3, Hv=4), 1), (dict(dv=32), 2),
+    (dict(dk=64), 2), (dict(chunk=32), 2), (dict(g=A + 4), 1), (dict(q=A + 8), 1),
+    (dict(scale=float("nan")), 1),
+])
+def test_kda_forward_rejects_bad_arguments(lib, case, status):
+    """KDA adds dk = 128 only and a 16-byte aligned per-channel gate to the forward's checks."""
+    assert fwd(lib, op="kda", **case) == status
+    assert lib.gdn_last_error() != b""
+
+
+def test_kda_step_rejects_bad_arguments(lib):
+    assert step(lib, op="kda", h=None) == 1
+    assert step(lib, op="kda", dk=80) == 2
+    assert step(lib, op="kda", N=0, q=None, k=None, v=None, g=None, beta=None, h=None,
+                o=None) == 0
+
+
+def test_kda_workspace_size_formula(lib):
+    # the GDN chunk record, then the fp16 Qt tile [64][dk] on a 128-byte line
+    def rec(dk, dv):
+        gv_end = 2 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 132 * 4
+        qt_off = (gv_end + 127) // 128 * 128
+        return (qt_off + 64 * dk * 2 + 127) // 128 * 128
+    assert lib.kda_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == \
+        64 * 16 * rec(128, 128)
+    assert lib.kda_chunk_fwd_workspace_size(8, 9849, 16, 32, 128, 64, 64, 1) == \
+        (9849 // 64 + 9) * 32 * rec(128, 64)
+    assert lib.kda_chunk_fwd_workspace_size(1, 64, 1, 1, 64, 128, 64, 0) == 0
