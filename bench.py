@@ -50,6 +50,8 @@ L2_FLUSH_BYTES = 320 * 2 ** 20
 # block times the call, and the launch list in profiles/ gives each kernel's share.
 KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
 LAUNCHES_PER_CALL = 2
+KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
+                "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)"}
 
 
 def kernel_source_hash() -> str:
@@ -136,7 +138,8 @@ class ClockSampler:
 
 def run_decode(lap, w, dev, steps=200):
     """µs per decode step on this workload's state shape, plain and as a CUDA graph."""
-    stepfn = lap.ssd_recurrent_step if w.op == "ssd" else lap.gdn_recurrent_step
+    stepfn = {"ssd": lap.ssd_recurrent_step, "kda": lap.kda_recurrent_step}.get(
+        w.op, lap.gdn_recurrent_step)
     N, Hv = w.n_seqs, w.Hv
     h = torch.randn((N, Hv, w.dk, w.dv), device=dev) * 0.1
     d = make_decode_inputs(w, 0, device=dev)
@@ -186,8 +189,8 @@ def run_decode(lap, w, dev, steps=200):
 
 def oracle_tokens_per_s(w, x_cpu, budget_s):
     """fp64 oracle (one core) on the first tokens of every head; returns (tok/s, sample)."""
-    from oracle import gdn_recurrent, ssd_recurrent
-    fwd = ssd_recurrent if w.op == "ssd" else gdn_recurrent
+    from oracle import gdn_recurrent, kda_recurrent, ssd_recurrent
+    fwd = {"ssd": ssd_recurrent, "kda": kda_recurrent}.get(w.op, gdn_recurrent)
     H = w.Hv
     # calibrate: a few tokens of every head
     probe = 16
@@ -248,7 +251,7 @@ def bench_cuda(args, w, rank, world, local_rank):
     o = torch.empty_like(x["v"])
     hT = torch.empty((w.n_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
 
-    fwd = lap.ssd_chunk_fwd if w.op == "ssd" else lap.gdn_chunk_fwd
+    fwd = {"ssd": lap.ssd_chunk_fwd, "kda": lap.kda_chunk_fwd}.get(w.op, lap.gdn_chunk_fwd)
 
     def step():
         fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
@@ -318,7 +321,8 @@ def bench_cuda(args, w, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic(w.name), "peak_source": src,
-                     "kernel": KERNEL_NAME, "algorithmic_bytes": model["bytes"],
+                     "kernel": KERNEL_NAMES.get(w.op, KERNEL_NAME),
+                     "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],
                      "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),
                      "t_roof_us": round(model["t_roof"] * 1e6, 2),

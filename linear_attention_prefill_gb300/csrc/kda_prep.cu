@@ -21,7 +21,8 @@
 // channel sum as GDN's scalar mask does; it is split around a reference token s
 // per 16-row block I of the chunk (s = 16 I + 7, the block's middle):
 //   A_ij = beta_i sum_c [k_ic exp(G_ic - G_sc)] [k_jc exp(G_sc - G_jc)],
-// one tf32 tensor-core product per block row.  For j < 16 I the right factor
+// one tf32 tensor-core product per block row (operands converted to tf32 once,
+// fragments read with ldmatrix).  For j < 16 I the right factor
 // is at most 1; within the block both factors stay within exp(8 max|g|), so
 // every factor is a normal fp32 number for log-decays down to about -10 per
 // token and channel (the input recipe draws g = -softplus(N(mu, 1)) s), and a
@@ -201,72 +202,89 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
   }
 
   // ---- #2 grams, one 16-row block row I at a time, channels in two halves ----------
+  // Warp w owns column tile w (8 columns) of block row I: the A and the P tile there
+  // share the B fragments of the column operand.
   __half* Pg = ws.P(slot, hv, p.Hv);
+  uint32_t* RKu = reinterpret_cast<uint32_t*>(RK);
+  uint32_t* RQu = reinterpret_cast<uint32_t*>(RQ);
+  uint32_t* Cu = reinterpret_cast<uint32_t*>(Cm);
   for (int I = 0; I < 4; ++I) {
     const int nc = 16 * (I + 1);  // columns 0 .. nc - 1
-    const int nt = nc / 8;        // n8 tiles of each gram
-    const int jobs = 2 * nt;      // A tiles, then P tiles: at most two per warp
     const int s = 16 * I + 7;     // reference token of the block row
-    float acc[2][4];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) acc[u][x] = 0.f;
+    float accA[4] = {0.f, 0.f, 0.f, 0.f}, accP[4] = {0.f, 0.f, 0.f, 0.f};
     for (int hf = 0; hf < 2; ++hf) {
       const int c0 = 64 * hf;
       __syncthreads();  // the scratch is free
       const float* Gref = Gs + s * kDK + c0;
-      for (int e = tid; e < 16 * 64; e += kThreads) {
-        const int i = e >> 6, cc = e & 63, j = 16 * I + i;
-        const float f = exp_of(Gs[j * kDK + c0 + cc] - Gref[cc]);
-        RK[i * kLd + cc] = __bfloat162float(Ks[swz<kDK>(j, c0 + cc)]) * f;
-        RQ[i * kLd + cc] = __bfloat162float(Qs[swz<kDK>(j, c0 + cc)]) * f;
-      }
-      for (int e = tid; e < nc * 64; e += kThreads) {
-        const int m = e >> 6, cc = e & 63;
-        Cm[m * kLd + cc] =
-            __bfloat162float(Ks[swz<kDK>(m, c0 + cc)]) * exp_of(Gref[cc] - Gs[m * kDK + c0 + cc]);
+      // operands in tf32, 8 channels an item: rows of block I (K and Q), then columns
+      for (int e = tid; e < 16 * 8 + nc * 8; e += kThreads) {
+        const bool row_item = e < 16 * 8;
+        const int r = row_item ? 16 * I + (e >> 3) : (e - 16 * 8) >> 3;
+        const int ch = e & 7, cb = c0 + 8 * ch;
+        float kf[8], f[8];
+        unpack_bf16x8(Ks + swz<kDK>(r, cb), kf);
+        const float4 ga = *reinterpret_cast<const float4*>(Gs + r * kDK + cb);
+        const float4 gb = *reinterpret_cast<const float4*>(Gs + r * kDK + cb + 4);
+        const float4 ra = *reinterpret_cast<const float4*>(Gref + 8 * ch);
+        const float4 rb = *reinterpret_cast<const float4*>(Gref + 8 * ch + 4);
+        const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+        const float r8[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+        // rows: exp(G_r - G_s); columns: exp(G_s - G_m)
+#pragma unroll
+        for (int x = 0; x < 8; ++x) f[x] = exp_of(row_item ? g8[x] - r8[x] : r8[x] - g8[x]);
+        uint32_t t[8];
+        if (row_item) {
+          const int i = e >> 3;
+          float qf[8];
+          unpack_bf16x8(Qs + swz<kDK>(r, cb), qf);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) t[x] = to_tf32(kf[x] * f[x]);
+          *reinterpret_cast<uint4*>(RKu + i * kLd + 8 * ch) = make_uint4(t[0], t[1], t[2], t[3]);
+          *reinterpret_cast<uint4*>(RKu + i * kLd + 8 * ch + 4) = make_uint4(t[4], t[5], t[6], t[7]);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) t[x] = to_tf32(qf[x] * f[x]);
+          *reinterpret_cast<uint4*>(RQu + i * kLd + 8 * ch) = make_uint4(t[0], t[1], t[2], t[3]);
+          *reinterpret_cast<uint4*>(RQu + i * kLd + 8 * ch + 4) = make_uint4(t[4], t[5], t[6], t[7]);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 8; ++x) t[x] = to_tf32(kf[x] * f[x]);
+          *reinterpret_cast<uint4*>(Cu + r * kLd + 8 * ch) = make_uint4(t[0], t[1], t[2], t[3]);
+          *reinterpret_cast<uint4*>(Cu + r * kLd + 8 * ch + 4) = make_uint4(t[4], t[5], t[6], t[7]);
+        }
       }
       __syncthreads();
+      if (warp < nc / 8) {
+        const int n0 = 8 * warp;
+        // ldmatrix on 32-bit elements: an 8x8 b16 matrix is 8 rows x 4 words, and thread
+        // t receives word t % 4 of row t / 4 - the tf32 fragment layout
+        const int arow = (lane & 7) + (((lane >> 3) & 1) << 3), aword = (lane >> 4) << 2;
+        const int brow = n0 + (lane & 7), bword = (lane >> 3) << 2;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int jb = warp + 8 * u;
-        if (jb < jobs) {
-          const bool isP = jb >= nt;
-          const int n0 = 8 * (isP ? jb - nt : jb);
-          const float* R = isP ? RQ : RK;
+        for (int k0 = 0; k0 < 64; k0 += 16) {
+          uint32_t b[4], ak[4], aq[4];
+          ldsm_x4(b[0], b[1], b[2], b[3], Cu + brow * kLd + k0 + bword);
 #pragma unroll
-          for (int k0 = 0; k0 < 64; k0 += 8) {
-            uint32_t a[4];
-            a[0] = to_tf32(R[gq * kLd + k0 + tq]);
-            a[1] = to_tf32(R[(gq + 8) * kLd + k0 + tq]);
-            a[2] = to_tf32(R[gq * kLd + k0 + tq + 4]);
-            a[3] = to_tf32(R[(gq + 8) * kLd + k0 + tq + 4]);
-            mma_tf32(acc[u], a, to_tf32(Cm[(n0 + gq) * kLd + k0 + tq]),
-                     to_tf32(Cm[(n0 + gq) * kLd + k0 + tq + 4]));
+          for (int h = 0; h < 2; ++h) {
+            const int kk = k0 + 8 * h;
+            ldsm_x4(ak[0], ak[1], ak[2], ak[3], RKu + arow * kLd + kk + aword);
+            ldsm_x4(aq[0], aq[1], aq[2], aq[3], RQu + arow * kLd + kk + aword);
+            mma_tf32(accA, ak, b[2 * h], b[2 * h + 1]);
+            mma_tf32(accP, aq, b[2 * h], b[2 * h + 1]);
           }
         }
       }
     }
     // block row I of A (fp32, shared) and P (fp16 record), masked to the triangles
+    if (warp < nc / 8) {
+      const int m = 8 * warp + 2 * tq;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int jb = warp + 8 * u;
-      if (jb < jobs) {
-        const bool isP = jb >= nt;
-        const int n0 = 8 * (isP ? jb - nt : jb);
-#pragma unroll
-        for (int xh = 0; xh < 2; ++xh) {
-          const int i = 16 * I + gq + 8 * xh, m = n0 + 2 * tq;
-          const float v0 = acc[u][2 * xh], v1 = acc[u][2 * xh + 1];
-          if (isP) {
-            *reinterpret_cast<uint32_t*>(Pg + swz<kC>(i, m)) =
-                pack_f16(m <= i ? p.scale * v0 : 0.f, m + 1 <= i ? p.scale * v1 : 0.f);
-          } else {
-            As[i * kC + m] = m < i ? s_beta[i] * v0 : 0.f;
-            As[i * kC + m + 1] = m + 1 < i ? s_beta[i] * v1 : 0.f;
-          }
-        }
+      for (int xh = 0; xh < 2; ++xh) {
+        const int i = 16 * I + gq + 8 * xh;
+        *reinterpret_cast<uint32_t*>(Pg + swz<kC>(i, m)) =
+            pack_f16(m <= i ? p.scale * accP[2 * xh] : 0.f,
+                     m + 1 <= i ? p.scale * accP[2 * xh + 1] : 0.f);
+        As[i * kC + m] = m < i ? s_beta[i] * accA[2 * xh] : 0.f;
+        As[i * kC + m + 1] = m + 1 < i ? s_beta[i] * accA[2 * xh + 1] : 0.f;
       }
     }
   }

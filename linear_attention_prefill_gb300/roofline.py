@@ -73,7 +73,8 @@ def ssd_macs_per_token_head(chunk, dk, dv):
 
 
 def flops(T_total, Hv, chunk, dk, dv, op="gdn"):
-    per = macs_per_token_head if op == "gdn" else ssd_macs_per_token_head
+    # KDA has GDN's products (its per-channel gate adds exponentials, not MACs)
+    per = ssd_macs_per_token_head if op == "ssd" else macs_per_token_head
     return 2.0 * T_total * Hv * per(chunk, dk, dv)
 
 
@@ -91,7 +92,8 @@ def workload_model(w, peaks):
     """Bytes, FLOPs and roofline time of one forward call of workload ``w``."""
     eb = 4 if w.dtype == "f32" else 2
     b = io_bytes(w.T_total, w.n_seqs, w.Hqk, w.Hv, w.dk, w.dv, eb,
-                 h0_read=w.h0_std is not None, hT_written=True)
+                 h0_read=w.h0_std is not None, hT_written=True,
+                 gate_per_channel=getattr(w, "op", "gdn") == "kda")
     f = flops(w.T_total, w.Hv, w.chunk, w.dk, w.dv, getattr(w, "op", "gdn"))
     t_hbm = b / (peaks["hbm_gbs"] * 1e9)
     if w.dtype == "f32":
