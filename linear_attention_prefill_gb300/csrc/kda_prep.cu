@@ -31,8 +31,8 @@
 //
 // Layout and work: one CTA of 256 threads per (chunk slot, v head), ~106 KB of
 // shared memory (two CTAs per SM); loads by cp.async (rows past the sequence
-// zero-filled), the grams on tf32 mma.sync, the solve in fp32 on the CUDA
-// cores (gdn_common.cuh), W^T and U^T on fp16 mma.sync.  No waits other than
+// zero-filled), the grams on tf32 mma.sync, the solve's diagonal blocks in fp32
+// and its merges on fp16 mma.sync, W^T and U^T on fp16 mma.sync.  No waits other than
 // cp.async groups and CTA barriers.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -51,16 +51,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int DV>
 struct KdaLayout {
   static constexpr int kK = 0;                  // bf16 [64][128] swz<128>; later K~ fp16
-  static constexpr int kQ = kK + kC * kDK * 2;  // bf16 [64][128] swz<128>; later Tb fp16 [64][64] swz<64>
-  static constexpr int kG = kQ + kC * kDK * 2;  // fp32 [64][128] G; later T fp32 [64][64], X [768]
-  static constexpr int kA = kG + kC * kDK * 4;  // fp32 [64][64] A (strictly lower part)
+  static constexpr int kQ = kK + kC * kDK * 2;  // bf16 [64][128] swz<128>; later Tb, Th fp16
+  static constexpr int kG = kQ + kC * kDK * 2;  // fp32 [64][128] G
+  static constexpr int kA = kG + kC * kDK * 4;  // A: fp32 diagonal blocks [4][16][16], fp16 Ah
   static constexpr int kS = kA + kC * kC * 4;   // RK, RQ [16][kLd], C [64][kLd] fp32; later V
   static constexpr int kSBytes = (16 + 16 + 64) * kLd * 4;
   static constexpr int kVec = kS + kSBytes;     // beta [64], column totals [128]
   static constexpr int kBytes = kVec + (kC + kDK) * 4;
   static constexpr int kAlloc = kBytes + 128;   // slack to align the base
   static_assert(kC * DV * 2 <= kSBytes, "V fits the scratch");
-  static_assert(kC * kC * 4 + 3 * 256 * 4 <= kC * kDK * 4, "T and X fit G's space");
 };
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -113,11 +112,11 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + Lo::kK);
   __half* Kh = reinterpret_cast<__half*>(sm + Lo::kK);   // K~ after the grams
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + Lo::kQ);
-  __half* Tb = reinterpret_cast<__half*>(sm + Lo::kQ);   // Tm diag(beta) after the grams
+  __half* Tb = reinterpret_cast<__half*>(sm + Lo::kQ);         // Tm diag(beta), after the grams
+  __half* Th = reinterpret_cast<__half*>(sm + Lo::kQ + 8192);  // Tm (fp16), after the grams
   float* Gs = reinterpret_cast<float*>(sm + Lo::kG);
-  float* Ts = Gs;                                        // Tm after the grams
-  float* Xs = Gs + kC * kC;
-  float* As = reinterpret_cast<float*>(sm + Lo::kA);
+  float* Ad = reinterpret_cast<float*>(sm + Lo::kA);            // diagonal blocks of A, fp32
+  __half* Ah = reinterpret_cast<__half*>(sm + Lo::kA + 4096);  // A, fp16 [64][64] swz<64>
   float* RK = reinterpret_cast<float*>(sm + Lo::kS);
   float* RQ = RK + 16 * kLd;
   float* Cm = RQ + 16 * kLd;
@@ -274,17 +273,25 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
         }
       }
     }
-    // block row I of A (fp32, shared) and P (fp16 record), masked to the triangles
+    // block row I of A (fp16 Ah, and the diagonal block in fp32) and of P (fp16
+    // record), masked to the triangles
     if (warp < nc / 8) {
       const int m = 8 * warp + 2 * tq;
+      const bool diag = warp >= 2 * I;  // column tile inside the diagonal block
 #pragma unroll
       for (int xh = 0; xh < 2; ++xh) {
         const int i = 16 * I + gq + 8 * xh;
         *reinterpret_cast<uint32_t*>(Pg + swz<kC>(i, m)) =
             pack_f16(m <= i ? p.scale * accP[2 * xh] : 0.f,
                      m + 1 <= i ? p.scale * accP[2 * xh + 1] : 0.f);
-        As[i * kC + m] = m < i ? s_beta[i] * accA[2 * xh] : 0.f;
-        As[i * kC + m + 1] = m + 1 < i ? s_beta[i] * accA[2 * xh + 1] : 0.f;
+        const float a0 = m < i ? s_beta[i] * accA[2 * xh] : 0.f;
+        const float a1 = m + 1 < i ? s_beta[i] * accA[2 * xh + 1] : 0.f;
+        *reinterpret_cast<uint32_t*>(Ah + swz<kC>(i, m)) = pack_f16(a0, a1);
+        if (diag) {
+          float* d = Ad + I * 256 + (i - 16 * I) * 16 + (m - 16 * I);
+          d[0] = a0;
+          d[1] = a1;
+        }
       }
     }
   }
@@ -306,16 +313,96 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
     cp_async16(Vh + swz<DV>(r, ch * 8), vg + ((ok ? t0 + r : t0) * p.Hv + hv) * DV + ch * 8, ok);
   }
   cp_async_commit();
-  __syncthreads();  // G is dead: its space takes Tm
 
-  // ---- #3 Solve: Tm = (I + A)^-1 in fp32; then Tb = Tm diag(beta) in fp16 -----------
-  solve_unit_lower_64_f32<kThreads>(As, kC, Ts, kC, Xs);  // ends with a barrier
-  for (int i = tid; i < kC * 8; i += kThreads) {
-    const int r = i >> 3, ch = i & 7;
-    float x[8];
+  // ---- #3 Solve: Tm = (I + A)^-1 as Th (fp16) and Tb = Tm diag(beta) (fp16) --------
+  // Diagonal 16x16 blocks in fp32 by right-looking substitution (warp b, lane l =
+  // column l of block b) while warps 4-7 zero the upper blocks; then the blocks
+  // below the diagonal by two levels of merges on fp16 mma.sync:
+  //   T10 = -(T11 A10) T00,  T32 = -(T33 A32) T22,  T[32:64, 0:32] = -(T_BB A_BA) T_AA.
+  if (warp < 4) {
+    if (lane < 16) {
+      const int b = warp, l = lane;
+      const float* Ab = Ad + b * 256;
+      float x[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = Ts[r * kC + ch * 8 + e] * s_beta[ch * 8 + e];
-    *reinterpret_cast<uint4*>(Tb + swz<kC>(r, ch * 8)) = pack8_f16(x);
+      for (int i = 0; i < 16; ++i) x[i] = (i == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m)
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Ab[i * 16 + m], x[m], x[i]);
+      const int cc = 16 * b + l;
+      const float fb = s_beta[cc];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        Th[swz<kC>(16 * b + i, cc)] = __float2half_rn(x[i]);
+        Tb[swz<kC>(16 * b + i, cc)] = __float2half_rn(x[i] * fb);
+      }
+    }
+  } else {
+    for (int e = tid - 128; e < kC * 8; e += 128) {  // 16-byte chunks of the upper blocks
+      const int rr = e >> 3, ch = e & 7;
+      if ((ch >> 1) > (rr >> 4)) {
+        *reinterpret_cast<uint4*>(Th + swz<kC>(rr, 8 * ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(Tb + swz<kC>(rr, 8 * ch)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < 2) {
+    // T(r, c), T(r, c + 1) -> Th (level 1 only) and Tb = T diag(beta)
+    auto put = [&](bool th, int r, int c, float t0, float t1) {
+      if (th) *reinterpret_cast<uint32_t*>(Th + swz<kC>(r, c)) = pack_f16(t0, t1);
+      *reinterpret_cast<uint32_t*>(Tb + swz<kC>(r, c)) =
+          pack_f16(t0 * s_beta[c], t1 * s_beta[c + 1]);
+    };
+    {  // level 1: warp 0 the block (1, 0), warp 1 the block (3, 2)
+      const int i0 = 16 + 32 * warp, j0 = 32 * warp;
+      float y[2][4] = {}, t[2][4] = {};
+      uint32_t a[4], b[4];
+      load_a_sw<kC>(a, Th, i0, i0, lane);     // T_II
+      load_b_kn_sw<kC>(b, Ah, j0, i0, lane);  // A_IJ as [k][n]
+      mma_f16(y[0], a, b[0], b[1]);
+      mma_f16(y[1], a, b[2], b[3]);
+      c_to_a(a, y[0], y[1]);
+      load_b_kn_sw<kC>(b, Th, j0, j0, lane);  // T_JJ as [k][n]
+      mma_f16(t[0], a, b[0], b[1]);
+      mma_f16(t[1], a, b[2], b[3]);
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int xh = 0; xh < 2; ++xh)
+          put(true, i0 + gq + 8 * xh, j0 + 8 * jn + 2 * tq, -t[jn][2 * xh], -t[jn][2 * xh + 1]);
+    }
+    named_sync(1, 64);
+    {  // level 2: rows 32..63 x columns 0..31; warp w takes 16 rows
+      const int i0 = 32 + 16 * warp;
+      float y[4][4] = {}, t[4][4] = {};
+      uint32_t a[4], b[4];
+      for (int k0 = 32; k0 <= i0; k0 += 16) {  // T_BB is lower triangular
+        load_a_sw<kC>(a, Th, i0, k0, lane);
+        load_b_kn_sw<kC>(b, Ah, 0, k0, lane);
+        mma_f16(y[0], a, b[0], b[1]);
+        mma_f16(y[1], a, b[2], b[3]);
+        load_b_kn_sw<kC>(b, Ah, 16, k0, lane);
+        mma_f16(y[2], a, b[0], b[1]);
+        mma_f16(y[3], a, b[2], b[3]);
+      }
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {  // k over the 32 columns of Y
+        c_to_a(a, y[2 * s2], y[2 * s2 + 1]);
+        load_b_kn_sw<kC>(b, Th, 0, 16 * s2, lane);
+        mma_f16(t[0], a, b[0], b[1]);
+        mma_f16(t[1], a, b[2], b[3]);
+        load_b_kn_sw<kC>(b, Th, 16, 16 * s2, lane);
+        mma_f16(t[2], a, b[0], b[1]);
+        mma_f16(t[3], a, b[2], b[3]);
+      }
+#pragma unroll
+      for (int jn = 0; jn < 4; ++jn)
+#pragma unroll
+        for (int xh = 0; xh < 2; ++xh)
+          put(false, i0 + gq + 8 * xh, 8 * jn + 2 * tq, -t[jn][2 * xh], -t[jn][2 * xh + 1]);
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
