@@ -180,7 +180,8 @@ def run_decode(lap, w, dev, steps=200):
         graph_us = a.elapsed_time(b) * 1e3 / (100 * (steps // 100))
     except RuntimeError:
         graph_us = None
-    nbytes = roofline.decode_bytes(N, w.Hqk, Hv, w.dk, w.dv, 2 if w.dtype == "bf16" else 4)
+    nbytes = roofline.decode_bytes(N, w.Hqk, Hv, w.dk, w.dv, 2 if w.dtype == "bf16" else 4,
+                                   gate_per_channel=w.op == "kda")
     return {"us_per_step": round(plain, 3),
             "us_per_step_cuda_graph": None if graph_us is None else round(graph_us, 3),
             "bytes_per_step": nbytes,

@@ -78,10 +78,12 @@ def flops(T_total, Hv, chunk, dk, dv, op="gdn"):
     return 2.0 * T_total * Hv * per(chunk, dk, dv)
 
 
-def decode_bytes(n_seqs, Hqk, Hv, dk, dv, elem_bytes):
-    """One decode step: the fp32 state read and written, plus one token of q, k, v, o, g, beta."""
+def decode_bytes(n_seqs, Hqk, Hv, dk, dv, elem_bytes, gate_per_channel=False):
+    """One decode step: the fp32 state read and written, plus one token of q, k, v, o, g, beta
+    (g per key channel for KDA)."""
     return (n_seqs * Hv * dk * dv * 4 * 2
-            + n_seqs * (2 * Hqk * dk + 2 * Hv * dv) * elem_bytes + n_seqs * Hv * 8)
+            + n_seqs * (2 * Hqk * dk + 2 * Hv * dv) * elem_bytes
+            + n_seqs * Hv * 4 * ((dk if gate_per_channel else 1) + 1))
 
 
 def fp32_alu_tflops(sm_mhz):
