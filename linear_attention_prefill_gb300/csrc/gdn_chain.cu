@@ -4,7 +4,7 @@
 // read and the in-place update:
 //   #5 read    V_new = U - W h
 //   #5 update  h = gamma_last h + Kt^T V_new        (Kt = diag(e) K)
-//   #6 O       O = diag(scale gamma) Q h + P V_new  (h: the state entering the chunk)
+//   #6 O       O = Q~ h + P V_new  (Q~ = diag(scale gamma) Q; h: the state entering the chunk)
 // One CTA per (sequence, v head, dv tile) walks the chunks of its sequence in
 // order with its fp32 state tile h[:, tile] in registers: the column split of
 // the state (§4, Figure 8(b)) gives parallelism without any reduction.
@@ -15,20 +15,19 @@
 // entering each chunk (fp16) and V_new in a 3-deep shared-memory ring, from
 // which warps 4-7 compute that chunk's output tile one or two chunks behind,
 // so neither ever travels through HBM.  Warp 8 is the producer: it stages W^T,
-// Kt, P, the U^T tile and the gate factors of chunk c + 3 with bulk copies and
-// the chunk's q rows with a TMA tensor load into a 3-deep ring.  The roles meet
-// only at mbarriers; every wait is bounded and an expired wait ends the CTA
-// cleanly.
+// Kt, P, the U^T tile, the gate factors and Q~ of chunk c + 3 with bulk copies
+// into a 3-deep ring.  The roles meet only at mbarriers; every wait is bounded
+// and an expired wait ends the CTA cleanly.
 //
-// Precision: every product takes fp16 operands with fp32 accumulation; the
-// output warps scale their bf16 q fragments by scale gamma_i and round them to
-// fp16 in registers, so q needs no converted copy anywhere.
+// Precision: every product takes fp16 operands with fp32 accumulation.  Q~ is
+// formed by the prep kernel (scale gamma_i, and the norm with the fused
+// prologue, applied to the bf16 q rows and rounded once to fp16), so the output
+// warps feed it to the tensor cores as it is.
 //
 // KDA mode (Kimi Delta Attention, the per-channel gate; records from
 // kda_prep.cu): the decay of the state update is one factor per state row,
-// h <- diag(exp G_last) h + Kt^T V_new, and the output's left factor
-// Q~ = scale Q * exp(G) varies per channel, so the producer stages the fp16 Q~
-// record instead of q and the output warps use it as it is.
+// h <- diag(exp G_last) h + Kt^T V_new, and Q~ = scale Q * exp(G) carries the
+// per-channel decay.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
@@ -47,8 +46,8 @@ constexpr int kPub = 3;  // state / V_new buffers shared with the output warps
 // Shared-memory map (byte offsets from a 1024-aligned base).
 template <int DK, int DVT>
 struct ChainLayout {
-  // one stage: q rows (bf16, 128-byte swizzle, [DK/64][64][64]) first for the
-  // 1024-byte alignment the swizzle needs, then the workspace record pieces
+  // one stage: the record's Q~ rows (fp16, swzb<64>: [DK/64][64][64], the
+  // 128-byte swizzle) first, then the other record pieces
   static constexpr int kQ = 0;
   static constexpr int kWt = kQ + kC * DK * 2;   // W^T [DK][64] swz<64>
   static constexpr int kKt = kWt + kC * DK * 2;  // Kt [64][DK] swzb<64>
@@ -72,15 +71,9 @@ __device__ __forceinline__ void load_a_sw128(uint32_t (&a)[4], const unsigned ch
           base + (k >> 6) * 8192 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-// bf16 pair times s, rounded once to an fp16 pair
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t x, float s) {
-  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x));
-  return pack_f16(f.x * s, f.y * s);
-}
-
 template <int DK, int DVT, bool KDA>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdn_chain_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq) {
+    gdn_chain_kernel(const FwdParams p, const WsLayout ws) {
   using Lo = ChainLayout<DK, DVT>;
   constexpr int NT = DVT / 8;          // n8 tiles over the dv tile
   constexpr int MTW = DK / 64;         // m16 tiles of the state per chain warp
@@ -105,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int dvt = blockIdx.x % n_dvt;
   const int hv = (blockIdx.x / n_dvt) % p.Hv;
   const int n = blockIdx.x / (n_dvt * p.Hv);
-  const int hq = hv / (p.Hv / p.Hqk);
   const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
   const long long len = p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
   const int n_chunks = (int)((len + kC - 1) / kC);
@@ -161,14 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_g2s(st + Lo::kP, ws.P(slot, hv, p.Hv), kC * kC * 2, bar);
         bulk_g2s(st + Lo::kUt, ws.U(slot, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
         bulk_g2s(st + Lo::kGv, ws.gv(slot, hv, p.Hv), kGvFloats * 4, bar);
-        if constexpr (KDA) {  // Q~, already in the q tile's layout
-          bulk_g2s(st + Lo::kQ, ws.Qt(slot, hv, p.Hv), kC * DK * 2, bar);
-        } else {
-          const int row = (int)(t_seq + (long long)c * kC);
-#pragma unroll
-          for (int kb = 0; kb < DK / 64; ++kb)
-            tma_load_2d(st + Lo::kQ + kb * 8192, &tmq, hq * DK + kb * 64, row, bar);
-        }
+        bulk_g2s(st + Lo::kQ, ws.Qt(slot, hv, p.Hv), kC * DK * 2, bar);
       };
       for (int c = 0; c < kStages && c < n_chunks; ++c) issue(c);
       for (int c = 0; c + kStages < n_chunks; ++c) {
@@ -200,20 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int x = 0; x < 4; ++x) acc[j][x] = 0.f;
-      // inter-chunk term (diag(scale gamma) Q) h: the bf16 q fragments of rows
-      // gq and gq + 8 are scaled and rounded to fp16 in registers
-      const float* gv = reinterpret_cast<const float*>(st + Lo::kGv);
-      const float s0 = p.scale * gv[4 + m0 + gq], s1 = p.scale * gv[4 + m0 + gq + 8];
+      // inter-chunk term Q~ h (Q~ already scaled, fp16)
 #pragma unroll
       for (int ks = 0; ks < DK / 16; ++ks) {
         uint32_t a[4];
         load_a_sw128(a, st + Lo::kQ, m0, 16 * ks, lane);
-        if constexpr (!KDA) {
-          a[0] = bf16x2_to_f16x2_scaled(a[0], s0);
-          a[1] = bf16x2_to_f16x2_scaled(a[1], s1);
-          a[2] = bf16x2_to_f16x2_scaled(a[2], s0);
-          a[3] = bf16x2_to_f16x2_scaled(a[3], s1);
-        }
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
           uint32_t bb[4];
@@ -399,16 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DK, int DVT>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
   using Lo = ChainLayout<DK, DVT>;
-  const long long rows = p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
-  CUtensorMap mq;
-  if (!make_tensor_map_bf16(&mq, p.q, rows, (long long)p.Hqk * DK)) return cudaErrorInvalidValue;
   const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
+  if (!ws.qrec) return cudaErrorInvalidValue;  // the chain reads Q~ from the records
   if (p.kda) {  // KDA records exist for dk = 128 only
     if constexpr (DK == 128) {
       cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, true>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
       if (e != cudaSuccess) return e;
-      gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
+      gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
       return cudaGetLastError();
     }
     return cudaErrorInvalidValue;
@@ -416,7 +390,7 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
   cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
   if (e != cudaSuccess) return e;
-  gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq);
+  gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
   return cudaGetLastError();
 }
 

@@ -68,11 +68,13 @@ struct StepParams {
 //                   tile j is the contiguous rows [j t, (j + 1) t)
 //   gv   fp32 [132] gamma_last, 3 pad, gamma_i = exp(G_i) for the 64 rows, then
 //                   e_j for the 64 rows (norm factors folded in with the prologue)
+//   Qt   [64][dk]   Q~ = diag(scale gamma) Q (norm folded in), swzb<64>, fp16: the
+//                   output's left factor, in the layout the chain stages q in
 // Kimi Delta Attention records (kda_prep.cu, dk = 128) are the same tiles with
 // the per-channel gate inside (W = Tm diag(beta) (K * exp G), Kt = K *
-// exp(G_last - G), P with exp(G_i - G_j) inside the channel sum), gv[4 + c] =
-// exp(G_last,c) for the 128 key channels, and one more tile:
-//   Qt   [64][dk]   scale Q * exp(G), swzb<64>, fp16 (the output's left factor)
+// exp(G_last - G), P with exp(G_i - G_j) inside the channel sum, Qt = scale Q *
+// exp(G)) and gv[4 + c] = exp(G_last,c) for the 128 key channels.
+// The block path (ws.blocks) reads q itself and its chunk records carry no Qt.
 // Every 16-bit tile is in the tensor cores' 128-byte-swizzled layout, so the
 // same bytes serve ldmatrix loads and tcgen05 operand descriptors.
 // The dv tile t (16 or 32 columns, one chain CTA each) is picked per call by
@@ -103,6 +105,7 @@ struct WsLayout {
   long long n_slots;        // chunk slots per v head
   long long slots_per_seq;  // fixed-length rows: ceil(T / 64); 0 with cu_seqlens
   long long task_bytes, kt_off, p_off, u_off, gv_off, qt_off;
+  int qrec;                 // 1: the records carry the Qt tile (every chunk-chain run)
   int blocks;               // 1: the block path runs (pair records present)
   long long n_bslots, bslots_per_seq, pair_off, pair_bytes, pb_off, ph_off, pg_off;
   // fused scan launch: [n_bslots][Hv] pair-done flags, [n_bslots][Hv][2]
@@ -195,9 +198,10 @@ inline WsLayout ws_layout(const FwdParams& p, void* base) {
   w.u_off = w.p_off + (long long)kChunk * kChunk * 2;
   w.gv_off = w.u_off + wv;
   w.qt_off = (w.gv_off + kGvFloats * 4 + 127) / 128 * 128;
-  // records on 128-byte lines; the KDA record adds the Qt tile
-  w.task_bytes = p.kda ? (w.qt_off + wk + 127) / 128 * 128 : w.qt_off;
   w.blocks = !p.kda && p.delta_rule && p.dk == 128 && p.dv == 128 && block_path_enabled();
+  // records on 128-byte lines; a chain run's records add the Qt tile
+  w.qrec = p.kda || !w.blocks;
+  w.task_bytes = w.qrec ? (w.qt_off + wk + 127) / 128 * 128 : w.qt_off;
   if (p.cu_seqlens) {
     w.bslots_per_seq = 0;
     w.n_bslots = (long long)p.T / kBlock + p.N + 1;

@@ -284,6 +284,16 @@ __global__ void __launch_bounds__(kThreads, 4)
       const unsigned char* src = sm + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(Kt + swzb<kC>(r, ch * 8)) = scale_bf16x8_to_f16(src, s_e[r]);
     }
+    if (ws.qrec) {  // the output's left factor diag(scale gamma) Q (norm folded in), fp16
+      __half* Qt = ws.Qt(slot, hv, p.Hv);
+      for (int i = tid; i < kC * kRowChunks; i += kThreads) {
+        const int r = i / kRowChunks, ch = i % kRowChunks;
+        const unsigned char* src =
+            sm + (ch >> 3) * 16384 + 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(Qt + swzb<kC>(r, ch * 8)) =
+            scale_bf16x8_to_f16(src, p.scale * s_gam[r] * s_rq[r]);
+      }
+    }
   }
   GDN_STAMP(33, 0);  // Kt written (thread 0's share)
   if (tid == 0 && !*s_abort && !mbar_wait(bar_mma, 0, p.err)) *s_abort = 1;

@@ -131,20 +131,29 @@ def test_product_path_does_not_import_the_oracle():
 
 def test_workspace_size_formula(lib):
     # chunk record: W^T [dk][64], Kt [64][dk], P [64][64], U^T [dv][64] (fp16), 132 fp32
-    # gate factors, padded to a 128-byte multiple
+    # gate factors on a 128-byte line, then the fp16 Q~ tile [64][dk] (not with the block
+    # path, which reads q itself), padded to a 128-byte multiple
+    block_path = os.environ.get("GDN_BLOCK_PATH") == "1"
+
     def rec(dk, dv):
         raw = 2 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 132 * 4
-        return (raw + 127) // 128 * 128
+        gv_end = (raw + 127) // 128 * 128
+        blocks = block_path and dk == 128 and dv == 128
+        return gv_end if blocks else (gv_end + 64 * dk * 2 + 127) // 128 * 128
     # block record (dk = dv = 128, block path on): N [dk][dk], B [dk][dv], H [dk][dv]
     # (fp16) and 16 bytes for the block's gate, padded to a 128-byte multiple
     blk = (128 * 128 * 2 * 3 + 16 + 127) // 128 * 128 if os.environ.get("GDN_BLOCK_PATH") == "1" else 0
+    # block path: per-block flags (pair done, two stored states) and a task counter
+    def flags(n_bslots, Hv):
+        return (n_bslots * Hv * 3 * 4 + 4 + 127) // 128 * 128 if blk else 0
     # fixed-length rows: N * ceil(T/64) chunk slots and N * ceil(T/128) block slots, x Hv
     assert lib.gdn_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == \
-        64 * 16 * rec(128, 128) + 32 * 16 * blk
+        64 * 16 * rec(128, 128) + 32 * 16 * blk + flags(32, 16)
     assert lib.gdn_chunk_fwd_workspace_size(2, 100, 1, 4, 128, 64, 64, 0) == 2 * 2 * 4 * rec(128, 64)
     # packed rows: floor(T/64) + N + 1 chunk slots, floor(T/128) + N + 1 block slots
+    nb = 9849 // 128 + 9
     assert lib.gdn_chunk_fwd_workspace_size(8, 9849, 16, 32, 128, 128, 64, 1) == \
-        (9849 // 64 + 9) * 32 * rec(128, 128) + (9849 // 128 + 9) * 32 * blk
+        (9849 // 64 + 9) * 32 * rec(128, 128) + nb * 32 * blk + flags(nb, 32)
     # rejected sizes give 0
     assert lib.gdn_chunk_fwd_workspace_size(1, 64, 3, 4, 128, 128, 64, 0) == 0
     assert lib.gdn_chunk_fwd_workspace_size(1, 64, 1, 1, 96, 128, 64, 0) == 0
