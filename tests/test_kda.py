@@ -121,3 +121,19 @@ def test_kda_decode_step_and_continuation(cuda_lib):
                                  cat(x["g"], g1), cat(x["beta"], b1), x["scale"], to_np(x["h0"]))
     assert rel_err(to_np(o1), o_all[:, -1], out_dtype="bf16") < TOL["bf16"]
     assert rel_err(to_np(h), h_all) < TOL["bf16"]
+
+
+def test_kda_gate_domain_edge(cuda_lib):
+    """Log-decays down to -10 per token and channel (the stated domain of the GPU path):
+    a tenth of the gate entries set to -10, runs of 8 strongly decaying tokens in some
+    channels, the rest weak; the grams' block-referenced factors must stay in range."""
+    x = make_inputs(kda_case(300, seed=90), device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(91)
+    g = x["g"] * 0.05
+    g = torch.where(torch.rand(g.shape, generator=gen, device="cuda") < 0.1,
+                    torch.full_like(g, -10.0), g)
+    g[:, 40:48, :, :16] = -10.0   # eight consecutive tokens, sixteen channels
+    x["g"] = g.contiguous()
+    o, hT = run(cuda_lib, x)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    check_heads(x, o, hT, heads=range(2), dtype="bf16", op="kda")
