@@ -62,12 +62,6 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src,
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gmem_src), "r"(n)
                : "memory");
 }
-__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src, bool valid) {
-  const uint32_t d = smem_u32(smem_dst);
-  const int n = valid ? 4 : 0;
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(d), "l"(gmem_src), "r"(n)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -210,52 +204,9 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// D = A * B + D, bf16 inputs, fp32 accumulation (for products of two bf16 inputs).
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// A fragment (16x16) of a row-major [m][k] bf16 tile at (m0, k0); ld in elements.
-__device__ __forceinline__ void load_a(uint32_t (&a)[4], const __half* base, int ld,
-                                       int m0, int k0, int lane) {
-  const __half* p = base + (m0 + (lane & 15)) * ld + k0 + ((lane >> 4) << 3);
-  ldsm_x4(a[0], a[1], a[2], a[3], p);
-}
-// A fragment (16x16) when the tile is stored transposed, as [k][m] (m contiguous).
-__device__ __forceinline__ void load_a_trans(uint32_t (&a)[4], const __half* base, int ld,
-                                             int m0, int k0, int lane) {
-  // Stored as [k][m]; lane groups 0-7, 8-15, 16-23, 24-31 address the four 8x8
-  // matrices a0 (m 0-7, k 0-7), a1 (m 8-15, k 0-7), a2 (m 0-7, k 8-15),
-  // a3 (m 8-15, k 8-15); each row address is one k row of 8 m values.
-  const int g = lane >> 3;
-  const int kr = k0 + (lane & 7) + ((g >> 1) << 3);
-  const int mc = m0 + ((g & 1) << 3);
-  ldsm_x4_t(a[0], a[1], a[2], a[3], base + kr * ld + mc);
-}
-// Two B fragments (k16 x n8 each, n tiles n0 and n0+8) of a tile stored as [n][k]
-// (k contiguous): b[0],b[1] for n0; b[2],b[3] for n0+8.
-__device__ __forceinline__ void load_b_nk(uint32_t (&b)[4], const __half* base, int ld,
-                                          int n0, int k0, int lane) {
-  const int g = lane >> 3;
-  const int nr = n0 + (lane & 7) + ((g >> 1) << 3);
-  const int kc = k0 + ((g & 1) << 3);
-  ldsm_x4(b[0], b[1], b[2], b[3], base + nr * ld + kc);
-}
-// Two B fragments of a tile stored as [k][n] (n contiguous).
-__device__ __forceinline__ void load_b_kn(uint32_t (&b)[4], const __half* base, int ld,
-                                          int n0, int k0, int lane) {
-  const int g = lane >> 3;
-  const int kr = k0 + (lane & 7) + ((g & 1) << 3);
-  const int nc = n0 + ((g >> 1) << 3);
-  ldsm_x4_t(b[0], b[1], b[2], b[3], base + kr * ld + nc);
-}
-
-// Swizzled-tile variants of the fragment loads (tile width W halves, see swz).
+// Fragment loads from swizzled tiles (tile width W halves, see swz): A fragments
+// (16x16) of [m][k] tiles, or of tiles stored transposed as [k][m]; pairs of B
+// fragments (k16 x n8, n tiles n0 and n0 + 8) of tiles stored as [k][n].
 template <int W>
 __device__ __forceinline__ void load_a_sw(uint32_t (&a)[4], const __half* base, int m0, int k0,
                                           int lane) {

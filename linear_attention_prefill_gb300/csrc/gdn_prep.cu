@@ -8,8 +8,9 @@
 //      QK^T   P = tril(scale exp(G_i - G_j) q_i.k_j)
 //   #3 Solve  Tm = (I + A)^-1   (diagonal blocks by substitution, merges on mma.sync)
 //   #4 W/U    W = Tm diag(beta gamma) K,  U = Tm diag(beta) V
-// plus the scaled copy Kt = diag(e) K (the state update's left factor) and
-// the row factors gamma.  The serial Reduce (#5) and the final Map (#6) run in
+// plus the scaled copies Kt = diag(e) K (the state update's left factor) and
+// Q~ = diag(scale gamma) Q (the output's left factor, fp16), and the row
+// factors gamma.  The serial Reduce (#5) and the final Map (#6) run in
 // gdn_chain.cu, which reads this kernel's workspace records.
 //
 // Blackwell mapping.  K and Q arrive by TMA in 128-byte-swizzled tiles stacked
