@@ -137,3 +137,12 @@ def test_kda_gate_domain_edge(cuda_lib):
     o, hT = run(cuda_lib, x)
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
     check_heads(x, o, hT, heads=range(2), dtype="bf16", op="kda")
+
+
+def test_kda_long_sequence_weak_decay(cuda_lib):
+    """16K tokens (256 chunks) with weak per-channel decay: the carried state stays accurate
+    over a long chain (one v head checked in full against the fp64 recurrence)."""
+    x = make_inputs(kda_case(16384, Hqk=1, Hv=2, seed=92, g_scale=0.02), device="cuda")
+    o, hT = run(cuda_lib, x)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    check_heads(x, o, hT, heads=[1], dtype="bf16", op="kda")
