@@ -51,7 +51,9 @@ L2_FLUSH_BYTES = 320 * 2 ** 20
 KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
 LAUNCHES_PER_CALL = 2
 KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
-                "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)"}
+                "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
+                "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
+                                "gdn_chain_kernel)"}
 
 
 def kernel_source_hash() -> str:
@@ -190,8 +192,12 @@ def run_decode(lap, w, dev, steps=200):
 
 def oracle_tokens_per_s(w, x_cpu, budget_s):
     """fp64 oracle (one core) on the first tokens of every head; returns (tok/s, sample)."""
-    from oracle import gdn_recurrent, kda_recurrent, ssd_recurrent
+    from oracle import gdn_recurrent, kda_recurrent, prologue, ssd_recurrent
     fwd = {"ssd": ssd_recurrent, "kda": kda_recurrent}.get(w.op, gdn_recurrent)
+    if w.prologue:  # the oracle's prologue, then the recurrence
+        def fwd(q, k, v, a, b, scale, h0, _f=fwd):
+            qn, kn, g, beta = prologue(q, k, a, b)
+            return _f(qn, kn, v, g, beta, scale, h0)
     H = w.Hv
     # calibrate: a few tokens of every head
     probe = 16
@@ -253,6 +259,9 @@ def bench_cuda(args, w, rank, world, local_rank):
     hT = torch.empty((w.n_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
 
     fwd = {"ssd": lap.ssd_chunk_fwd, "kda": lap.kda_chunk_fwd}.get(w.op, lap.gdn_chunk_fwd)
+    if w.prologue:  # raw q, k and gate inputs through the fused prologue
+        def fwd(q, k, v, a, b, h0, o, hT, **kw):
+            return lap.gdn_chunk_fwd_prologue(q, k, v, a, b, None, None, h0, o, hT, **kw)
 
     def step():
         fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
@@ -290,7 +299,8 @@ def bench_cuda(args, w, rank, world, local_rank):
     # one overlaps the compute and download of the previous (HostPipeline)
     host = {k_: (None if x[k_] is None else x[k_].detach().cpu().pin_memory())
             for k_ in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")}
-    pipe = lap.HostPipeline(chunk=w.chunk, device=dev, op=w.op, depth=2)
+    pipe = lap.HostPipeline(chunk=w.chunk, device=dev,
+                            op="gdn_prologue" if w.prologue else w.op, depth=2)
     for _ in range(max(2, args.warmup)):
         pipe.submit(host)
     torch.cuda.synchronize()
@@ -322,7 +332,8 @@ def bench_cuda(args, w, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic(w.name), "peak_source": src,
-                     "kernel": KERNEL_NAMES.get(w.op, KERNEL_NAME),
+                     "kernel": KERNEL_NAMES.get("gdn_prologue" if w.prologue else w.op,
+                                               KERNEL_NAME),
                      "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],
                      "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),

@@ -321,7 +321,8 @@ def gdn_device_status(stream=None):
 def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None,
                        op: str = "gdn"):
     """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out
-    (``op`` "ssd" runs ssd_chunk_fwd, "kda" kda_chunk_fwd instead).
+    (``op`` "ssd" runs ssd_chunk_fwd, "kda" kda_chunk_fwd, "gdn_prologue"
+    gdn_chunk_fwd_prologue on raw q, k and gate inputs instead).
 
     ``inputs`` holds pinned CPU tensors q, k, v, g, beta and optionally h0 and
     cu_seqlens.  ``out`` may hold preallocated pinned (o, hT) host tensors and
@@ -342,7 +343,9 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         buf.copy_(t, non_blocking=True)
         d[name] = buf
         nbytes_in += t.numel() * t.element_size()
-    fwd = {"ssd": ssd_chunk_fwd, "kda": kda_chunk_fwd}.get(op, gdn_chunk_fwd)
+    fwd = {"ssd": ssd_chunk_fwd, "kda": kda_chunk_fwd,
+           "gdn_prologue": lambda q, k, v, a, b, h0, o, hT, **kw: gdn_chunk_fwd_prologue(
+               q, k, v, a, b, None, None, h0, o, hT, **kw)}.get(op, gdn_chunk_fwd)
     if "workspace" not in bufs:
         B, T, Hqk, dk = d["q"].shape
         Hv, dv = d["v"].shape[2], d["v"].shape[3]

@@ -51,6 +51,7 @@ class Workload:
     varlen: bool = False    # True: one packed [1, T_total, ...] batch with cu_seqlens
     seed: int = 0
     decode_steps: int = 0   # one-token steps that continue from the final state
+    prologue: bool = False  # raw inputs for the fused prologue (see make_inputs)
 
     @property
     def T_total(self) -> int:
@@ -98,6 +99,11 @@ WORKLOADS["long_64k_weak_c128"] = WORKLOADS["long_64k_weak"].replace(
 
 # Mamba-2 SSD scan of a 2.7B-class model ("Exp 2026-07-13 — Linear-Attention Scans on the
 # NPU", §3: head_dim 64, d_state 128, chunks of 64; 80 heads sharing one B/C group), 4K prompt.
+# The headline layer fed raw: unnormalised q, k and the gate inputs a, b of the fused
+# prologue (g = -softplus(a), beta = sigmoid(b): the same distributions as the headline).
+WORKLOADS["layer_16h_4k_prologue"] = WORKLOADS["layer_16h_4k"].replace(
+    name="layer_16h_4k_prologue", prologue=True)
+
 WORKLOADS["ssd_80h_4k"] = Workload("ssd_80h_4k", (4096,), 1, 80, 128, 64, 64, "bf16", seed=6,
                                    op="ssd")
 
@@ -128,7 +134,8 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
     """Draw one batch of inputs for workload ``w`` on ``device``.
 
     Returns a dict with q, k ([B, T, Hqk, dk]), v ([B, T, Hv, dv]), g ([B, T, Hv]
-    fp32, or [B, T, Hv, dk] for KDA), beta ([B, T, Hv] fp32), h0 ([N, Hv, dk, dv] fp32 or None), cu_seqlens (int32
+    fp32, or [B, T, Hv, dk] for KDA), beta ([B, T, Hv] fp32) - for a prologue workload
+    q, k unnormalised and g, beta the raw gate inputs a, b - h0 ([N, Hv, dk, dv] fp32 or None), cu_seqlens (int32
     [N+1] on ``device`` for varlen workloads, else None), and the sizes
     B, T, N, scale.  A varlen batch is one packed row: B = N sequences,
     tensors [1, T_total, ...].
@@ -146,10 +153,17 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> dict:
     def randn(*shape):
         return torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
 
-    q = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
-    k = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
+    if w.prologue:  # raw rows: N(0, 1) times a per-row factor exp(N(0, 1))
+        q = (randn(B, T, w.Hqk, w.dk) * torch.exp(randn(B, T, w.Hqk, 1))).to(dt)
+        k = (randn(B, T, w.Hqk, w.dk) * torch.exp(randn(B, T, w.Hqk, 1))).to(dt)
+    else:
+        q = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
+        k = _unit_rows(randn(B, T, w.Hqk, w.dk)).to(dt)
     v = randn(B, T, w.Hv, w.dv).to(dt)
-    if w.op == "ssd":
+    if w.prologue:  # the raw gate inputs a (in g) and b (in beta)
+        beta = randn(B, T, w.Hv)
+        g = randn(B, T, w.Hv) + w.g_mu
+    elif w.op == "ssd":
         # dt = softplus(N(0, 1)) is the input step (beta); g = dt * A with A = -exp(N(0, 0.3))
         # per head
         beta = torch.nn.functional.softplus(randn(B, T, w.Hv))
