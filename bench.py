@@ -45,15 +45,39 @@ from linear_attention_prefill_gb300.workloads import HEADLINE, WORKLOADS, make_d
 METRIC = "GDN chunked-prefill tokens/s per layer on 1 GB300; % of TC/HBM roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 320 * 2 ** 20
-# One gdn_chunk_fwd call is two launches on the caller's stream (the chunk-parallel
-# prep kernel, then the chunk-serial chain kernel that also writes o); the roofline
-# block times the call, and the launch list in profiles/ gives each kernel's share.
+# One bf16 forward call is two launches on the caller's stream (the chunk-parallel
+# prep kernel, then the chunk-serial chain kernel that also writes o); the fp32 path
+# is one fused launch.  The roofline block times the call, and the launch list in
+# profiles/ gives each kernel's share.
 KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
-LAUNCHES_PER_CALL = 2
 KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
                 "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
                 "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
-                                "gdn_chain_kernel)"}
+                                "gdn_chain_kernel)",
+                "f32": "gdn_chunk_fwd_f32 (gdn_fwd_f32_kernel)",
+                "ssd_f32": "ssd_chunk_fwd_f32 (gdn_fwd_f32_kernel, no erase term)"}
+
+
+def kernel_name(w) -> str:
+    if w.dtype == "f32":
+        return KERNEL_NAMES["ssd_f32" if w.op == "ssd" else "f32"]
+    return KERNEL_NAMES.get("gdn_prologue" if w.prologue else w.op, KERNEL_NAME)
+
+
+def launches_per_call(w) -> int:
+    """Kernel launches of one forward call: the fp32 path is one fused launch; the bf16
+    path prep + chain, or with the opt-in 128-token block path prep + the fused block
+    launch (four launches where the fused one does not apply: packed rows or too many
+    chains for the SMs)."""
+    if w.dtype == "f32":
+        return 1
+    block = (os.environ.get("GDN_BLOCK_PATH") == "1" and w.op == "gdn" and w.dk == 128
+             and w.dv == 128)
+    if not block:
+        return 2
+    fused = not w.varlen and w.n_seqs * w.Hv * 2 <= torch.cuda.get_device_properties(
+        torch.cuda.current_device()).multi_processor_count - 32
+    return 2 if fused else 4
 
 
 def kernel_source_hash() -> str:
@@ -292,7 +316,7 @@ def bench_cuda(args, w, rank, world, local_rank):
     local_ms = sum(ms)
     job_ms, job_tokens = reduce_timing(local_ms, float(w.T_total * args.steps))
     value = job_tokens / (job_ms / 1e3)
-    launches = LAUNCHES_PER_CALL * args.steps
+    launches = launches_per_call(w) * args.steps
 
     # end to end through the public API from pinned host memory: every step copies its
     # inputs in and o, hT out; consecutive steps run on two streams so the upload of
@@ -332,8 +356,7 @@ def bench_cuda(args, w, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic(w.name), "peak_source": src,
-                     "kernel": KERNEL_NAMES.get("gdn_prologue" if w.prologue else w.op,
-                                               KERNEL_NAME),
+                     "kernel": kernel_name(w),
                      "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],
                      "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),
