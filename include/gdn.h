@@ -260,7 +260,8 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
  *   g     [B, T, Hv, dk] fp32, one log-decay per key channel, 16-byte aligned;
  *         exact to the tolerance for g >= -10 per token and channel (the chunk
  *         grams split exp(G_i - G_j) around each 16-token block's middle token,
- *         and a factor must stay a normal fp32 number)
+ *         and a factor must stay a normal fp32 number); a value below -10 (or
+ *         NaN) is reported by the next gdn_device_status as GDN_ERR_INVALID_ARG
  *   dk    128 only (GDN_ERR_UNSUPPORTED otherwise); dv 64 or 128
  * kda_chunk_fwd_ex takes a caller-owned device workspace of at least
  * kda_chunk_fwd_workspace_size(...) bytes, 256-byte aligned (0 for rejected
@@ -285,8 +286,11 @@ gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const
 
 /*
  * gdn_device_status - waits for `stream`, then reads and clears the device
- * error word that bounded device-side waits set when they give up.  Returns
- * GDN_OK, GDN_ERR_TIMEOUT, or GDN_ERR_CUDA if the stream itself failed.
+ * error word that bounded device-side waits set when they give up, and that
+ * the KDA forward sets when a log-decay is below -10 or not a number.  Returns
+ * GDN_OK, GDN_ERR_TIMEOUT, GDN_ERR_INVALID_ARG (a KDA gate outside its range:
+ * the result of that call is not exact), or GDN_ERR_CUDA if the stream itself
+ * failed.
  */
 gdn_status gdn_device_status(gdn_stream_t stream);
 

@@ -313,7 +313,8 @@ def gdn_selftest_expired_wait(limit_cycles: int = 1 << 20, stream=None):
 
 
 def gdn_device_status(stream=None):
-    """Raise GdnError if a bounded device-side wait gave up since the last check."""
+    """Raise GdnError if a bounded device-side wait gave up since the last check
+    (GDN_ERR_TIMEOUT), or a KDA log-decay lay below -10 (GDN_ERR_INVALID_ARG)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     _check(load_library().gdn_device_status(_stream_handle(stream, dev)))
 

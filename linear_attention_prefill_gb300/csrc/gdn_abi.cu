@@ -484,6 +484,9 @@ gdn_status gdn_device_status(gdn_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
   if (word == gdn::kErrWaitTimeout)
     return fail(GDN_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (word == gdn::kErrGateRange)
+    return fail(GDN_ERR_INVALID_ARG,
+                "a KDA log-decay was below -10 or not a number: that call's result is not exact");
   if (word != 0u) return fail(GDN_ERR_TIMEOUT, "device error word 0x%x", word);
   return GDN_OK;
 }

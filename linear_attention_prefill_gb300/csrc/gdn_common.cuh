@@ -48,8 +48,9 @@ extern __device__ unsigned long long g_gdn_phase[64];  // defined in gdn_abi.cu;
 
 namespace gdn {
 
-// Device error word: bounded waits record why they gave up (read by gdn_device_status).
-enum : unsigned { kErrNone = 0u, kErrWaitTimeout = 1u };
+// Device error word (read by gdn_device_status): a bounded wait gave up, or a KDA
+// log-decay lay outside the range the KDA forward is exact for.
+enum : unsigned { kErrNone = 0u, kErrWaitTimeout = 1u, kErrGateRange = 2u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -46,6 +46,7 @@ constexpr int kThreads = 256;
 constexpr int kDK = 128;  // key head dim: the gate's channels
 constexpr int kLd = 68;   // fp32 operand row stride: conflict-free tf32 fragment loads
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMinGate = -10.f;  // the grams' factors stay in fp32 range down to here
 
 // Shared-memory map (byte offsets from a 128-aligned base).
 template <int DV>
@@ -162,8 +163,13 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
   {
     const int ch = tid % kDK, half = tid / kDK;
     float x[32];
+    bool in_range = true;  // false for a log-decay below kMinGate or not a number
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = Gs[(32 * half + i) * kDK + ch];
+    for (int i = 0; i < 32; ++i) {
+      x[i] = Gs[(32 * half + i) * kDK + ch];
+      in_range = in_range && x[i] >= kMinGate;
+    }
+    if (!in_range && p.err) atomicExch(p.err, kErrGateRange);
 #pragma unroll
     for (int i = 1; i < 32; ++i) x[i] += x[i - 1];
     if (half == 0) s_tot[ch] = x[31];

@@ -146,3 +146,19 @@ def test_kda_long_sequence_weak_decay(cuda_lib):
     o, hT = run(cuda_lib, x)
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
     check_heads(x, o, hT, heads=[1], dtype="bf16", op="kda")
+
+
+def test_kda_gate_outside_range_is_reported(cuda_lib):
+    """A log-decay below -10 is outside the range the GPU path is exact for: the prep
+    records it in the device error word and gdn_device_status reports INVALID_ARG once;
+    an in-range call afterwards reports nothing."""
+    cuda_lib.gdn_device_status()  # clear anything earlier
+    x = make_inputs(kda_case(130, seed=93), device="cuda")
+    g = x["g"].clone()
+    g[0, 70, 1, 5] = -12.0
+    run(cuda_lib, dict(x, g=g.contiguous()))
+    with pytest.raises(cuda_lib.GdnError) as err:
+        cuda_lib.gdn_device_status()
+    assert err.value.status == 1  # GDN_ERR_INVALID_ARG
+    run(cuda_lib, x)
+    cuda_lib.gdn_device_status()  # in range: no report
