@@ -43,14 +43,15 @@ constexpr int kThreads = 288;
 constexpr int kStages = 3;
 constexpr int kPub = 3;  // state / V_new buffers shared with the output warps
 
-// Shared-memory map (byte offsets from a 1024-aligned base).
-template <int DK, int DVT>
+// Shared-memory map (byte offsets from a 1024-aligned base).  NOW: a run without
+// the erase term (Mamba-2 SSD), whose stages carry no W tile.
+template <int DK, int DVT, bool NOW = false>
 struct ChainLayout {
   // one stage: the record's Q~ rows (fp16, swzb<64>: [DK/64][64][64], the
   // 128-byte swizzle) first, then the other record pieces
   static constexpr int kQ = 0;
   static constexpr int kWt = kQ + kC * DK * 2;   // W^T [DK][64] swz<64>
-  static constexpr int kKt = kWt + kC * DK * 2;  // Kt [64][DK] swzb<64>
+  static constexpr int kKt = kWt + (NOW ? 0 : kC * DK * 2);  // Kt [64][DK] swzb<64>
   static constexpr int kP = kKt + kC * DK * 2;   // P [64][64] swz<64>
   static constexpr int kUt = kP + kC * kC * 2;   // U^T [DVT][64] swz<64>
   static constexpr int kGv = kUt + DVT * kC * 2; // gamma_last, pad, gamma[64], e[64]
@@ -60,7 +61,8 @@ struct ChainLayout {
   static constexpr int kBar = kVn + kPub * kC * DVT * 2;
   static constexpr int kBytes = kBar + 8 * (2 * kStages + 2 * kPub) + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base
-  static constexpr unsigned kTx = 3 * kC * DK * 2 + kC * kC * 2 + DVT * kC * 2 + kGvFloats * 4;
+  static constexpr unsigned kTx =
+      (NOW ? 2 : 3) * kC * DK * 2 + kC * kC * 2 + DVT * kC * 2 + kGvFloats * 4;
 };
 
 // A fragment (16x16) of a bf16 tile in the 128-byte-swizzled [k/64][rows][64] layout.
@@ -71,10 +73,11 @@ __device__ __forceinline__ void load_a_sw128(uint32_t (&a)[4], const unsigned ch
           base + (k >> 6) * 8192 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-template <int DK, int DVT, bool KDA>
+template <int DK, int DVT, bool KDA, bool NOW = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chain_kernel(const FwdParams p, const WsLayout ws) {
-  using Lo = ChainLayout<DK, DVT>;
+  using Lo = ChainLayout<DK, DVT, NOW>;
+  const bool delta = !NOW && p.delta_rule;  // the erase term (W) takes part
   constexpr int NT = DVT / 8;          // n8 tiles over the dv tile
   constexpr int MTW = DK / 64;         // m16 tiles of the state per chain warp
   extern __shared__ unsigned char smem_raw[];
@@ -147,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* bar = &full[c % kStages];
         const long long slot = slot0 + c;
         // without the erase term (SSD) W is zero: it is neither formed nor loaded
-        mbar_expect_tx(bar, p.delta_rule ? Lo::kTx : Lo::kTx - kC * DK * 2);
-        if (p.delta_rule) bulk_g2s(st + Lo::kWt, ws.W(slot, hv, p.Hv), kC * DK * 2, bar);
+        mbar_expect_tx(bar, (delta || NOW) ? Lo::kTx : Lo::kTx - kC * DK * 2);
+        if (delta) bulk_g2s(st + Lo::kWt, ws.W(slot, hv, p.Hv), kC * DK * 2, bar);
         bulk_g2s(st + Lo::kKt, ws.Kt(slot, hv, p.Hv), kC * DK * 2, bar);
         bulk_g2s(st + Lo::kP, ws.P(slot, hv, p.Hv), kC * kC * 2, bar);
         bulk_g2s(st + Lo::kUt, ws.U(slot, hv, p.Hv) + dvt * kC * DVT, kC * DVT * 2, bar);
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(&full[c % kStages], (c / kStages) & 1, p.err)) *s_abort = 1;
     GDN_PHASE(17);  // wait for staging
     uint32_t wa[DK / 16][4];  // W rows of this warp, all k steps
-    if (p.delta_rule) {
+    if (delta) {
 #pragma unroll
       for (int ks = 0; ks < DK / 16; ++ks) load_a_trans_sw<kC>(wa[ks], Wt, 16 * warp, 16 * ks, lane);
     }
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int x = 0; x < 4; ++x) wh[hh][j][x] = 0.f;
-      if (p.delta_rule) {  // SSD: V_new = U
+      if (delta) {  // SSD: V_new = U
 #pragma unroll
       for (int ks = 0; ks < DK / 32; ++ks) {
 #pragma unroll
@@ -377,26 +380,37 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
   using Lo = ChainLayout<DK, DVT>;
   const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
   if (!ws.qrec) return cudaErrorInvalidValue;  // the chain reads Q~ from the records
-  if (p.kda) {  // KDA records exist for dk = 128 only
-    if constexpr (DK == 128) {
-      cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, true>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
-      if (e != cudaSuccess) return e;
-      gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
-      return cudaGetLastError();
+  if constexpr (DVT == 64) {  // 64-column tiles: only without the erase term (no W stage)
+    using L64 = ChainLayout<DK, 64, true>;
+    if (p.delta_rule || p.kda) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, 64, false, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L64::kAlloc);
+    if (e != cudaSuccess) return e;
+    gdn_chain_kernel<DK, 64, false, true><<<(unsigned)grid, kThreads, L64::kAlloc, stream>>>(p, ws);
+    return cudaGetLastError();
+  } else {
+    if (p.kda) {  // KDA records exist for dk = 128 only
+      if constexpr (DK == 128) {
+        cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
+        if (e != cudaSuccess) return e;
+        gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
+        return cudaGetLastError();
+      }
+      return cudaErrorInvalidValue;
     }
-    return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
+    if (e != cudaSuccess) return e;
+    gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
+    return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
-  if (e != cudaSuccess) return e;
-  gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
-  return cudaGetLastError();
 }
 
 template <int DK>
 cudaError_t launch_dk(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
   if (ws.dvt == 16) return launch_t<DK, 16>(p, ws, stream);
+  if (ws.dvt == 64) return launch_t<DK, 64>(p, ws, stream);
   return launch_t<DK, 32>(p, ws, stream);
 }
 

@@ -169,10 +169,13 @@ struct WsLayout {
 };
 
 // dv tile of the chain launch: 16 columns while chains x dv/16 CTAs fit on the
-// 152 SMs, else 32 (and never wider than dv).
+// 152 SMs, else 32 (and never wider than dv); without the erase term (no W stage)
+// a 64-column tile where 32-column CTAs would need a second wave but whole-dv
+// ones fit (dv = 64).
 inline int dv_tile(const FwdParams& p) {
   const long long chains = (long long)p.N * p.Hv;
   if (chains * (p.dv / 16) <= 152) return 16;
+  if (!p.delta_rule && !p.kda && p.dv == 64 && chains * 2 > 152 && chains <= 152) return 64;
   return 32;
 }
 

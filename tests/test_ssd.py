@@ -82,3 +82,13 @@ def test_ssd_decode_step(cuda_lib, dtype):
     o_ref, h_ref = ssd_step(q, k, v, g, beta, h_in, 1.0)
     assert rel_err(to_np(o), o_ref, out_dtype=dtype) < TOL[dtype]
     assert rel_err(to_np(h), h_ref) < TOL[dtype]
+
+
+def test_ssd_many_heads_whole_dv_tile(cuda_lib):
+    """80 heads of head_dim 64 (the 2.7B-class layer's shape): 32-column chain CTAs would
+    need a second wave, so the chain runs one 64-column CTA per head (no W stage);
+    heads sampled across the range."""
+    w = Workload("case", (300,), 1, 80, 128, 64, 64, "bf16", h0_std=0.1, seed=50)
+    x = ssd_inputs(w, 50)
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=[0, 37, 79], dtype="bf16", op="ssd")
