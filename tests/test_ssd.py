@@ -92,3 +92,12 @@ def test_ssd_many_heads_whole_dv_tile(cuda_lib):
     x = ssd_inputs(w, 50)
     o, hT = run(cuda_lib, x)
     check_heads(x, o, hT, heads=[0, 37, 79], dtype="bf16", op="ssd")
+
+
+def test_ssd_whole_dv_tile_varlen_groups(cuda_lib):
+    """The 64-column chain on packed rows: two sequences (one ragged) x 40 heads in
+    four B/C groups, with initial state."""
+    w = Workload("case", (130, 77), 4, 40, 128, 64, 64, "bf16", h0_std=0.1, varlen=True, seed=51)
+    x = ssd_inputs(w, 51)
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=[0, 13, 39], seqs=[0, 1], dtype="bf16", op="ssd")
