@@ -162,3 +162,10 @@ def test_kda_gate_outside_range_is_reported(cuda_lib):
     assert err.value.status == 1  # GDN_ERR_INVALID_ARG
     run(cuda_lib, x)
     cuda_lib.gdn_device_status()  # in range: no report
+
+
+def test_kda_32_column_chain_tile(cuda_lib):
+    """32 v heads: the KDA chain runs 32-column tiles (128 CTAs)."""
+    x = make_inputs(kda_case(150, Hqk=8, Hv=32, seed=94), device="cuda")
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=[0, 15, 31], dtype="bf16", op="kda")

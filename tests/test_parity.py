@@ -215,3 +215,13 @@ def test_allocating_entry_point_matches_workspace_entry_point(cuda_lib):
     torch.cuda.synchronize()
     assert rc == 0
     assert torch.equal(o, o_ref) and torch.equal(h, h_ref)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64)])
+def test_many_heads_take_the_32_column_chain_tile(cuda_lib, dk, dv):
+    """40 v heads of dv = 64: 160 CTAs of 16 columns would not fit the SMs, so the chain
+    runs 32-column tiles (the instantiations the workloads reach only at dk = dv = 128)."""
+    w = Workload("case", (150,), 4, 40, dk, dv, 64, "bf16", h0_std=0.1, seed=30 + dk)
+    x = make_inputs(w, device="cuda")
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=[0, 17, 39], dtype="bf16")
