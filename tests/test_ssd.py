@@ -101,3 +101,11 @@ def test_ssd_whole_dv_tile_varlen_groups(cuda_lib):
     x = ssd_inputs(w, 51)
     o, hT = run(cuda_lib, x)
     check_heads(x, o, hT, heads=[0, 13, 39], seqs=[0, 1], dtype="bf16", op="ssd")
+
+
+def test_ssd_whole_dv_tile_state_64(cuda_lib):
+    """The 64-column chain at d_state 64 (80 heads, one B/C group)."""
+    w = Workload("case", (200,), 1, 80, 64, 64, 64, "bf16", h0_std=0.1, seed=52)
+    x = ssd_inputs(w, 52)
+    o, hT = run(cuda_lib, x)
+    check_heads(x, o, hT, heads=[3, 44, 79], dtype="bf16", op="ssd")
