@@ -169,3 +169,23 @@ def test_kda_32_column_chain_tile(cuda_lib):
     x = make_inputs(kda_case(150, Hqk=8, Hv=32, seed=94), device="cuda")
     o, hT = run(cuda_lib, x)
     check_heads(x, o, hT, heads=[0, 15, 31], dtype="bf16", op="kda")
+
+
+@pytest.mark.parametrize("dk", [64, 128])
+def test_kda_decode_step_head_dims(cuda_lib, dk):
+    """The decode step against the oracle's step at both key head dims (GQA, dv = 64)."""
+    gen = torch.Generator(device="cuda").manual_seed(95 + dk)
+    N, Hqk, Hv, dv = 3, 2, 4, 64
+    unit = lambda x: torch.nn.functional.normalize(x, dim=-1).to(torch.bfloat16)
+    q = unit(torch.randn(N, Hqk, dk, generator=gen, device="cuda"))
+    k = unit(torch.randn(N, Hqk, dk, generator=gen, device="cuda"))
+    v = torch.randn(N, Hv, dv, generator=gen, device="cuda").to(torch.bfloat16)
+    g = -torch.nn.functional.softplus(torch.randn(N, Hv, dk, generator=gen, device="cuda"))
+    b = torch.sigmoid(torch.randn(N, Hv, generator=gen, device="cuda"))
+    h = torch.randn(N, Hv, dk, dv, generator=gen, device="cuda") * 0.1
+    h_in = h.clone()
+    o = cuda_lib.kda_recurrent_step(q, k, v, g.contiguous(), b.contiguous(), h)
+    o_ref, h_ref = kda_step(to_np(q), to_np(k), to_np(v), to_np(g), to_np(b), to_np(h_in),
+                            dk ** -0.5)
+    assert rel_err(to_np(o), o_ref, out_dtype="bf16") < TOL["bf16"]
+    assert rel_err(to_np(h), h_ref) < 1e-5
