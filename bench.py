@@ -49,11 +49,11 @@ L2_FLUSH_BYTES = 320 * 2 ** 20
 # prep kernel, then the chunk-serial chain kernel that also writes o); the fp32 path
 # is one fused launch.  The roofline block times the call, and the launch list in
 # profiles/ gives each kernel's share.
-KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
-KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
+KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_tc_kernel)"
+KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_tc_kernel, no erase term)",
                 "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
                 "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
-                                "gdn_chain_kernel)",
+                                "gdn_chain_tc_kernel)",
                 "f32": "gdn_chunk_fwd_f32 (gdn_fwd_f32_kernel)",
                 "ssd_f32": "ssd_chunk_fwd_f32 (gdn_fwd_f32_kernel, no erase term)"}
 
@@ -66,18 +66,8 @@ def kernel_name(w) -> str:
 
 def launches_per_call(w) -> int:
     """Kernel launches of one forward call: the fp32 path is one fused launch; the bf16
-    path prep + chain, or with the opt-in 128-token block path prep + the fused block
-    launch (four launches where the fused one does not apply: packed rows or too many
-    chains for the SMs)."""
-    if w.dtype == "f32":
-        return 1
-    block = (os.environ.get("GDN_BLOCK_PATH") == "1" and w.op == "gdn" and w.dk == 128
-             and w.dv == 128)
-    if not block:
-        return 2
-    fused = not w.varlen and w.n_seqs * w.Hv * 2 <= torch.cuda.get_device_properties(
-        torch.cuda.current_device()).multi_processor_count - 32
-    return 2 if fused else 4
+    path a prep launch and a chain launch."""
+    return 1 if w.dtype == "f32" else 2
 
 
 def kernel_source_hash() -> str:

@@ -23,19 +23,23 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  GDN_OK means the launch was enqueued.  Kernel faults
  *    show up on the stream like any CUDA error.
- *  - GQA: value head hv reads query/key head hv / (Hv / Hqk) ("grouped").
- *  - q and k are expected L2-normalised per head vector, beta in (0, 1) and
- *    g <= 0 (a log-decay); these are not checked.
+ *  - GQA: value head hv reads query/key head hv / (Hv / Hqk) ("grouped");
+ *    gdn_chunk_fwd_ex and gdn_recurrent_step_ex also take hv % Hqk ("modulo",
+ *    GDN_FLAG_HEAD_MAP_MODULO).
+ *  - q and k are expected L2-normalised per head vector, beta in [0, 1] and
+ *    g <= 0 (a log-decay).  The host does not read them; GDN_FLAG_CHECK_INPUTS
+ *    of the _ex entry points adds a device pass that checks g, beta and
+ *    cu_seqlens and reports a violation through gdn_device_status.
+ *  - Range of the bf16 path: the on-chip products take fp16 operands (the
+ *    state entering each chunk, V_new = U - W h and the scaled copies of q, k
+ *    and v are rounded to fp16 once), so |v|, the state and V_new must stay
+ *    below fp16's 65504.  A value outside that range (or not a number) in the
+ *    state or V_new is recorded and reported by the next gdn_device_status as
+ *    GDN_ERR_INVALID_ARG: that call's result is not exact.
  *  - Errors: a non-OK status means nothing was launched (except GDN_ERR_CUDA,
  *    which reports a failed launch).  gdn_last_error() gives a one-line
  *    description, per calling thread.  Nothing prints, aborts or throws.
- *  - Environment: GDN_BLOCK_PATH=1, read once when the library is first used,
- *    runs the bf16 gated-delta-rule forward at dk = dv = 128 on 128-token
- *    blocks (two chunks' state maps composed into one, the state walked with
- *    one tensor-core product per block, the block outputs in parallel); the
- *    result is the same function within the same tolerances, and
- *    gdn_chunk_fwd_workspace_size grows accordingly.  Unset (the default), the
- *    forward walks 64-token chunks, which is faster on GB300.
+ *  - No environment variable or other process state changes what a call does.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -48,6 +52,27 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* gdn_stream_t; /* ABI-identical to cudaStream_t */
+
+/* Flags of the _ex entry points (gdn_chunk_fwd_ex, gdn_chunk_fwd_prologue_ex,
+ * ssd_chunk_fwd_ex, kda_chunk_fwd_ex, gdn_recurrent_step_ex): bitwise or, 0 = the
+ * plain call.  An unknown bit is GDN_ERR_INVALID_ARG. */
+enum {
+  /* GQA map hv % Hqk instead of hv / (Hv / Hqk) (the replication of the GQA
+   * marshaller in "Exp 2026-07-13 — Linear-Attention Scans on the NPU", §4) */
+  GDN_FLAG_HEAD_MAP_MODULO = 1u,
+  /* before the forward (or step), one device pass checks every g <= 0 and
+   * finite, every beta in [0, 1], and cu_seqlens running from 0 to T without
+   * going down; a violation is reported by the next gdn_device_status as
+   * GDN_ERR_INVALID_ARG (the call itself still runs) */
+  GDN_FLAG_CHECK_INPUTS = 2u,
+  /* the chunk-serial operators on the 5th-generation tensor cores with the
+   * fp32 state resident in tensor memory: one CTA per (sequence, v head), the
+   * one-chunk lookahead form of the state read (the forwards' _ex entry points;
+   * KDA returns GDN_ERR_UNSUPPORTED).  Same function and tolerances; uses one SM
+   * per chain where the default uses dv / 16 (or 32), so it pays off when many
+   * chains share the GPU. */
+  GDN_FLAG_TC_CHAIN = 4u
+};
 
 typedef enum {
   GDN_OK = 0,
@@ -91,29 +116,32 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
 
 /*
  * gdn_chunk_fwd_workspace_size - bytes of device workspace gdn_chunk_fwd_ex
- * needs for these sizes (has_cu_seqlens: 1 if cu_seqlens will be passed).
- * The bf16 forward runs in two launches: the chunk-parallel operators #1-#4
- * (Gate, KKT, Solve, W/U) write one record per (64-token chunk, v head) -
- * W^T, diag(e) K, P and U^T in fp16 plus the gate factors, 57.7 KB at
- * d = 128 - and the chunk-serial launch (#5 H with #6 O) reads them.  Returns 0
- * for sizes gdn_chunk_fwd would reject.
+ * needs for these sizes with any flags (has_cu_seqlens: 1 if cu_seqlens will
+ * be passed).  The bf16 forward runs in two launches: the chunk-parallel
+ * operators #1-#4 (Gate, KKT, Solve, W/U) write one record per (64-token
+ * chunk, v head) - W, diag(e) K, P, U^T and diag(scale gamma) Q in fp16 plus
+ * the gate factors (72.6 KiB at d = 128; 80.6 KiB with GDN_FLAG_TC_CHAIN, whose
+ * records add the lookahead tile X) - and the chunk-serial launch (#5 H with
+ * #6 O) reads them.  Returns 0 for sizes gdn_chunk_fwd would reject.
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
                                     int has_cu_seqlens);
 
 /*
- * gdn_chunk_fwd_ex - gdn_chunk_fwd with a caller-provided device workspace of
- * at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte aligned.  The
+ * gdn_chunk_fwd_ex - gdn_chunk_fwd with `flags` (GDN_FLAG_*: the GQA map, the
+ * input check, the tensor-memory chain) and a caller-provided device workspace
+ * of at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte aligned.  The
  * workspace is overwritten; calls sharing it must be ordered on one stream.
- * Returns GDN_ERR_INVALID_ARG if it is NULL, misaligned or too small.
- * (gdn_chunk_fwd itself takes the workspace from the device's stream-ordered
- * memory pool with cudaMallocAsync/cudaFreeAsync on `stream`.)
+ * Returns GDN_ERR_INVALID_ARG if it is NULL, misaligned or too small, or for
+ * an unknown flag bit.  (gdn_chunk_fwd itself takes the workspace from the
+ * device's stream-ordered memory pool with cudaMallocAsync/cudaFreeAsync on
+ * `stream`.)
  */
 gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream);
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream);
 
 /*
  * gdn_chunk_fwd_noalloc - gdn_chunk_fwd for callers that must not allocate
@@ -129,9 +157,10 @@ gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const f
  *    nothing.
  *  - Every GPU that runs the library's device code keeps those 32 MiB until
  *    the process exits.
- *  - The first call on each device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ *    device also loads the library's device code there, so make it before any
+ *    stream capture.
  *  - All calls share the one array and its contents persist between calls;
  *    each call rewrites every byte it later reads, so nothing needs clearing,
  *    but calls that overlap on the GPU (different streams, or different host
@@ -163,6 +192,16 @@ gdn_status gdn_chunk_fwd_f32(const float* q, const float* k, const float* v, con
 gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
                               const float* beta, float* h, void* o, int N, int Hqk, int Hv,
                               int dk, int dv, float scale, gdn_stream_t stream);
+
+/*
+ * gdn_recurrent_step_ex - gdn_recurrent_step with `flags`:
+ * GDN_FLAG_HEAD_MAP_MODULO (the GQA map, as the prefill that produced h used)
+ * and GDN_FLAG_CHECK_INPUTS (g and beta of this token checked on the device).
+ */
+gdn_status gdn_recurrent_step_ex(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                                 int dk, int dv, float scale, unsigned flags,
+                                 gdn_stream_t stream);
 
 /* gdn_recurrent_step_f32 - as gdn_recurrent_step with fp32 q, k, v and o. */
 gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v,
@@ -196,7 +235,7 @@ gdn_status gdn_chunk_fwd_prologue_ex(const void* q, const void* k, const void* v
                                      const float* b, const float* A_log, const float* dt_bias,
                                      const float* h0, void* o, float* hT, int B, int T, int Hqk,
                                      int Hv, int dk, int dv, int chunk, float scale,
-                                     const int32_t* cu_seqlens, void* workspace,
+                                     const int32_t* cu_seqlens, unsigned flags, void* workspace,
                                      size_t workspace_bytes, gdn_stream_t stream);
 gdn_status gdn_recurrent_step_prologue(const void* q, const void* k, const void* v,
                                        const float* a, const float* b, const float* A_log,
@@ -227,8 +266,8 @@ gdn_status ssd_chunk_fwd(const void* q, const void* k, const void* v, const floa
 gdn_status ssd_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream);
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream);
 gdn_status ssd_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
                              const float* beta, const float* h0, float* o, float* hT, int B,
                              int T, int Hqk, int Hv, int dk, int dv, int chunk, float scale,
@@ -276,8 +315,8 @@ gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
 gdn_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream);
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream);
 size_t kda_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
                                     int has_cu_seqlens);
 gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g,
@@ -286,11 +325,12 @@ gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const
 
 /*
  * gdn_device_status - waits for `stream`, then reads and clears the device
- * error word that bounded device-side waits set when they give up, and that
- * the KDA forward sets when a log-decay is below -10 or not a number.  Returns
- * GDN_OK, GDN_ERR_TIMEOUT, GDN_ERR_INVALID_ARG (a KDA gate outside its range:
- * the result of that call is not exact), or GDN_ERR_CUDA if the stream itself
- * failed.
+ * error word.  The kernels record there (the first record stays until read):
+ * a bounded device-side wait that gave up (GDN_ERR_TIMEOUT); a KDA log-decay
+ * below -10 or not a number, an fp16 operand of the bf16 path out of range, or
+ * a violation found by GDN_FLAG_CHECK_INPUTS (GDN_ERR_INVALID_ARG: the result
+ * of that call is not exact).  Returns GDN_OK, one of those, or GDN_ERR_CUDA
+ * if the stream itself failed.
  */
 gdn_status gdn_device_status(gdn_stream_t stream);
 
@@ -311,7 +351,7 @@ const char* gdn_status_string(gdn_status s);
 /* Description of the last non-OK status returned to this thread ("" if none). */
 const char* gdn_last_error(void);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2. */
 int gdn_abi_version(void);
 
 #ifdef __cplusplus

@@ -19,30 +19,34 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(5)
+# flags of gdn_chunk_fwd_ex / gdn_recurrent_step_ex (include/gdn.h)
+GDN_FLAG_HEAD_MAP_MODULO, GDN_FLAG_CHECK_INPUTS, GDN_FLAG_TC_CHAIN = 1, 2, 4
 
 # name -> (restype, argtypes) of every symbol include/gdn.h declares
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 _FWD_ARGS = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]
 _STEP_ARGS = [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]
 _SZ = ctypes.c_size_t
+_U = ctypes.c_uint
 SIGNATURES = {
     "gdn_chunk_fwd": (_I, _FWD_ARGS),
-    "gdn_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "gdn_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_U, _P, _SZ, _P]),
     "gdn_chunk_fwd_noalloc": (_I, _FWD_ARGS),
     "gdn_chunk_fwd_workspace_size": (_SZ, [_I] * 8),
     "gdn_chunk_fwd_f32": (_I, _FWD_ARGS),
     "gdn_recurrent_step": (_I, _STEP_ARGS),
+    "gdn_recurrent_step_ex": (_I, _STEP_ARGS[:-1] + [_U, _P]),
     "gdn_recurrent_step_f32": (_I, _STEP_ARGS),
     "gdn_chunk_fwd_prologue": (_I, _FWD_ARGS[:5] + [_P, _P] + _FWD_ARGS[5:]),
-    "gdn_chunk_fwd_prologue_ex": (_I, _FWD_ARGS[:5] + [_P, _P] + _FWD_ARGS[5:-1] + [_P, _SZ, _P]),
+    "gdn_chunk_fwd_prologue_ex": (_I, _FWD_ARGS[:5] + [_P, _P] + _FWD_ARGS[5:-1] + [_U, _P, _SZ, _P]),
     "gdn_recurrent_step_prologue": (_I, _STEP_ARGS[:5] + [_P, _P] + _STEP_ARGS[5:]),
     "ssd_chunk_fwd": (_I, _FWD_ARGS),
-    "ssd_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "ssd_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_U, _P, _SZ, _P]),
     "ssd_chunk_fwd_f32": (_I, _FWD_ARGS),
     "ssd_recurrent_step": (_I, _STEP_ARGS),
     "ssd_recurrent_step_f32": (_I, _STEP_ARGS),
     "kda_chunk_fwd": (_I, _FWD_ARGS),
-    "kda_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_P, _SZ, _P]),
+    "kda_chunk_fwd_ex": (_I, _FWD_ARGS[:-1] + [_U, _P, _SZ, _P]),
     "kda_chunk_fwd_workspace_size": (_SZ, [_I] * 8),
     "kda_recurrent_step": (_I, _STEP_ARGS),
     "gdn_device_status": (_I, [_P]),
@@ -120,7 +124,8 @@ def gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) 
 
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
-                  stream=None, workspace=None):
+                  stream=None, workspace=None, head_map: str = "grouped",
+                  check_inputs: bool = False, tc_chain: bool = False):
     """Chunked-prefill forward of the gated delta rule; returns (o, hT).
 
     q, k [B, T, Hqk, dk]; v [B, T, Hv, dv] (bf16 or fp32, all the same);
@@ -129,16 +134,33 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
     o and hT may be passed preallocated; hT may be h0 (in place).  The bf16
     path runs gdn_chunk_fwd_ex with ``workspace`` (a uint8 device tensor of at
     least gdn_chunk_fwd_workspace_size bytes) or a fresh one from torch's
-    caching allocator.  ``scale`` defaults to dk^-0.5.
+    caching allocator, and the flags: ``head_map`` "grouped" (hv // (Hv // Hqk))
+    or "modulo" (hv % Hqk), ``check_inputs`` (a device pass over g, beta and
+    cu_seqlens, reported by gdn_device_status), ``tc_chain`` (the chunk-serial
+    operators on tcgen05 with the state in tensor memory).  ``scale`` defaults
+    to dk^-0.5.
     """
+    flags = _flags(head_map, check_inputs, tc_chain)
+    if flags and q.dtype != torch.bfloat16:
+        raise TypeError("head_map, check_inputs and tc_chain apply to the bf16 forward")
     return _chunk_fwd("gdn", q, k, v, g, beta, h0, o, hT, chunk,
                       k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
-                      output_final_state, stream, workspace)
+                      output_final_state, stream, workspace, flags=flags)
+
+
+def _flags(head_map="grouped", check_inputs=False, tc_chain=False) -> int:
+    if head_map not in ("grouped", "modulo"):
+        raise ValueError(f"head_map must be 'grouped' or 'modulo', got {head_map!r}")
+    return ((GDN_FLAG_HEAD_MAP_MODULO if head_map == "modulo" else 0)
+            | (GDN_FLAG_CHECK_INPUTS if check_inputs else 0)
+            | (GDN_FLAG_TC_CHAIN if tc_chain else 0))
 
 
 def gdn_chunk_fwd_prologue(q, k, v, a, b, A_log=None, dt_bias=None, h0=None, o=None, hT=None, *,
                            chunk: int = 64, scale: Optional[float] = None, cu_seqlens=None,
-                           output_final_state=True, stream=None, workspace=None):
+                           output_final_state=True, stream=None, workspace=None,
+                           head_map: str = "grouped", check_inputs: bool = False,
+                           tc_chain: bool = False):
     """gdn_chunk_fwd with the fused prologue (bf16): q, k unnormalised; raw gates a, b
     [B, T, Hv] fp32; A_log, dt_bias [Hv] fp32 or None.  g = -exp(A_log) softplus(a +
     dt_bias), beta = sigmoid(b), q and k divided by sqrt(sum x^2 + 1e-6).  Returns (o, hT)."""
@@ -149,18 +171,23 @@ def gdn_chunk_fwd_prologue(q, k, v, a, b, A_log=None, dt_bias=None, h0=None, o=N
             _need(t, name, torch.float32, dev, (Hv,))
     return _chunk_fwd("gdn", q, k, v, a, b, h0, o, hT, chunk,
                       k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
-                      output_final_state, stream, workspace, prologue=(A_log, dt_bias))
+                      output_final_state, stream, workspace, prologue=(A_log, dt_bias),
+                      flags=_flags(head_map, check_inputs, tc_chain))
 
 
 def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: float = 1.0, cu_seqlens=None, output_final_state=True, stream=None,
-                  workspace=None):
+                  workspace=None, head_map: str = "grouped", check_inputs: bool = False,
+                  tc_chain: bool = False):
     """Chunked Mamba-2 SSD scan (the same recurrence without the erase term):
     S_t = exp(g_t) S_{t-1} + beta_t v_t k_t^T, o_t = S_t (scale q_t), with
     C -> q, B -> k, x -> v, dt A -> g, dt -> beta.  Arguments as gdn_chunk_fwd;
     ``scale`` defaults to 1.  Returns (o, hT)."""
+    flags = _flags(head_map, check_inputs, tc_chain)
+    if flags and q.dtype != torch.bfloat16:
+        raise TypeError("head_map, check_inputs and tc_chain apply to the bf16 forward")
     return _chunk_fwd("ssd", q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens,
-                      output_final_state, stream, workspace)
+                      output_final_state, stream, workspace, flags=flags)
 
 
 def kda_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) -> int:
@@ -171,7 +198,8 @@ def kda_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) 
 
 def kda_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
-                  stream=None, workspace=None):
+                  stream=None, workspace=None, head_map: str = "grouped",
+                  check_inputs: bool = False):
     """Chunked-prefill forward of Kimi Delta Attention (bf16, dk = 128); returns (o, hT).
 
     h_t = (I - beta_t k_t k_t^T) diag(exp g_t) h_{t-1} + beta_t k_t v_t^T,
@@ -181,11 +209,12 @@ def kda_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
     """
     return _chunk_fwd("kda", q, k, v, g, beta, h0, o, hT, chunk,
                       k.shape[-1] ** -0.5 if scale is None else scale, cu_seqlens,
-                      output_final_state, stream, workspace)
+                      output_final_state, stream, workspace,
+                      flags=_flags(head_map, check_inputs))
 
 
 def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output_final_state,
-               stream, workspace, prologue=None):
+               stream, workspace, prologue=None, flags=0):
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":
@@ -228,8 +257,8 @@ def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         _need(workspace, "workspace", torch.uint8, dev)
-        _check(lib.gdn_chunk_fwd_prologue_ex(*args, _ptr(workspace), workspace.numel(),
-                                             _stream_handle(stream, dev)))
+        _check(lib.gdn_chunk_fwd_prologue_ex(*args, int(flags), _ptr(workspace),
+                                             workspace.numel(), _stream_handle(stream, dev)))
         return o, hT
     if dt == torch.float32:
         _check(getattr(lib, f"{op}_chunk_fwd_f32")(*args, _stream_handle(stream, dev)))
@@ -239,19 +268,23 @@ def _chunk_fwd(op, q, k, v, g, beta, h0, o, hT, chunk, scale, cu_seqlens, output
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
-    _check(getattr(lib, f"{op}_chunk_fwd_ex")(*args, _ptr(workspace), workspace.numel(),
-                                              _stream_handle(stream, dev)))
+    _check(getattr(lib, f"{op}_chunk_fwd_ex")(*args, int(flags), _ptr(workspace),
+                                              workspace.numel(), _stream_handle(stream, dev)))
     return o, hT
 
 
 def gdn_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = None,
-                       stream=None):
+                       stream=None, head_map: str = "grouped", check_inputs: bool = False):
     """One decode token of the gated delta rule; updates h in place and returns o.
 
     q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv] fp32; h [N, Hv, dk, dv] fp32.
+    ``head_map`` and ``check_inputs`` as in gdn_chunk_fwd (bf16: gdn_recurrent_step_ex).
     """
+    flags = _flags(head_map, check_inputs)
+    if flags and q.dtype != torch.bfloat16:
+        raise TypeError("head_map and check_inputs apply to the bf16 step")
     return _step("gdn", q, k, v, g, beta, h, o, k.shape[-1] ** -0.5 if scale is None else scale,
-                 stream)
+                 stream, flags=flags)
 
 
 def gdn_recurrent_step_prologue(q, k, v, a, b, h, A_log=None, dt_bias=None, o=None, *,
@@ -275,7 +308,7 @@ def kda_recurrent_step(q, k, v, g, beta, h, o=None, *, scale: Optional[float] = 
                  stream)
 
 
-def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None):
+def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None, flags=0):
     lib = load_library()
     dev = q.device
     dt = q.dtype
@@ -300,6 +333,11 @@ def _step(op, q, k, v, g, beta, h, o, scale, stream, prologue=None):
             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(prologue[0]), _ptr(prologue[1]),
             _ptr(h), _ptr(o), N, Hqk, Hv, dk, dv, float(scale), _stream_handle(stream, dev)))
         return o
+    if flags:
+        _check(lib.gdn_recurrent_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h),
+                                         _ptr(o), N, Hqk, Hv, dk, dv, float(scale), int(flags),
+                                         _stream_handle(stream, dev)))
+        return o
     fn = getattr(lib, f"{op}_recurrent_step" + ("" if dt == torch.bfloat16 else "_f32"))
     _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h), _ptr(o), N, Hqk, Hv,
               dk, dv, float(scale), _stream_handle(stream, dev)))
@@ -313,8 +351,9 @@ def gdn_selftest_expired_wait(limit_cycles: int = 1 << 20, stream=None):
 
 
 def gdn_device_status(stream=None):
-    """Raise GdnError if a bounded device-side wait gave up since the last check
-    (GDN_ERR_TIMEOUT), or a KDA log-decay lay below -10 (GDN_ERR_INVALID_ARG)."""
+    """Raise GdnError for what the kernels recorded since the last check: a bounded
+    device-side wait that gave up (GDN_ERR_TIMEOUT); a KDA log-decay below -10, an fp16
+    operand out of range, or an input-check violation (GDN_ERR_INVALID_ARG)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     _check(load_library().gdn_device_status(_stream_handle(stream, dev)))
 

@@ -7,8 +7,6 @@
 #include <stdio.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
@@ -20,14 +18,6 @@ __device__ unsigned long long g_gdn_phase[64];
 namespace gdn {
 
 __device__ unsigned g_device_error = 0u;
-
-bool block_path_enabled() {
-  static const bool on = [] {
-    const char* v = getenv("GDN_BLOCK_PATH");
-    return v && v[0] == '1' && v[1] == 0;
-  }();
-  return on;
-}
 
 cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
   unsigned zero = 0u;
@@ -52,6 +42,45 @@ __global__ void selftest_expired_wait_kernel(unsigned* err, long long limit) {
   }
   __syncwarp();
   if (threadIdx.x == 0) mbar_wait_limit(&bar, 0, err, limit);
+}
+
+// Input check of an _ex call: every log-decay g <= 0 and finite (with the fused
+// prologue the raw gate only finite), every beta in [0, 1] (raw: finite), and
+// cu_seqlens running from 0 to T without going down.  The first violation records
+// kErrInput in the error word; nothing is modified.
+__global__ void check_inputs_kernel(const float* g, long long n_g, const float* beta, long long n_b,
+                                    const int32_t* cu, int N, int T, int raw, unsigned* err) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  bool ok = true;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_g; i += stride) {
+    const float x = g[i];
+    ok &= raw ? isfinite(x) : (isfinite(x) && x <= 0.f);
+  }
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_b; i += stride) {
+    const float x = beta[i];
+    ok &= raw ? isfinite(x) : (x >= 0.f && x <= 1.f);
+  }
+  if (cu) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i <= N; i += stride) {
+      const int a = cu[i];
+      if (i == 0) ok &= a == 0;
+      if (i == N) ok &= a == T;
+      if (i > 0) ok &= a >= cu[i - 1];
+    }
+  }
+  if (!ok) record_error(err, kErrInput);
+}
+
+cudaError_t launch_check_inputs(const FwdParams& p, cudaStream_t stream) {
+  const long long rows = p.cu_seqlens ? 1ll : (long long)p.N;
+  const long long n_b = rows * p.T * p.Hv;
+  const long long n_g = n_b * (p.kda ? p.dk : 1);
+  int blocks = (int)((n_g + 255) / 256);
+  if (blocks > 1216) blocks = 1216;
+  if (blocks < 1) blocks = 1;
+  check_inputs_kernel<<<blocks, 256, 0, stream>>>(p.g, n_g, p.beta, n_b, p.cu_seqlens, p.N, p.T,
+                                                  p.prologue, p.err);
+  return cudaGetLastError();
 }
 
 }  // namespace gdn
@@ -116,6 +145,21 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   p->A_log = nullptr;
   p->dt_bias = nullptr;
   p->kda = 0;
+  p->head_map = 0;
+  p->tc_chain = 0;
+  return GDN_OK;
+}
+
+constexpr unsigned kFwdFlags = GDN_FLAG_HEAD_MAP_MODULO | GDN_FLAG_CHECK_INPUTS | GDN_FLAG_TC_CHAIN;
+
+// Applies the flags of an _ex forward to p; `tc_ok` says whether the tcgen05 chain
+// exists for this operation.
+gdn_status apply_flags(unsigned flags, bool tc_ok, gdn::FwdParams* p) {
+  if (flags & ~kFwdFlags) return fail(GDN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kFwdFlags);
+  if ((flags & GDN_FLAG_TC_CHAIN) && !tc_ok)
+    return fail(GDN_ERR_UNSUPPORTED, "GDN_FLAG_TC_CHAIN: no tensor-memory chain for this operation");
+  p->head_map = (flags & GDN_FLAG_HEAD_MAP_MODULO) ? 1 : 0;
+  p->tc_chain = (flags & GDN_FLAG_TC_CHAIN) ? 1 : 0;
   return GDN_OK;
 }
 
@@ -153,6 +197,7 @@ gdn_status check_step(const void* q, const void* k, const void* v, const float* 
   p->A_log = nullptr;
   p->dt_bias = nullptr;
   p->kda = 0;
+  p->head_map = 0;
   return GDN_OK;
 }
 
@@ -183,7 +228,8 @@ gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cuda
 
 // bf16 forward: the chunk-parallel prep launch, then the chunk-serial chain launch
 // (which also writes the output).
-gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaStream_t stream) {
+gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaStream_t stream,
+                        bool check = false) {
   if (p.N == 0) return GDN_OK;
   if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
   // tensor-map row coordinates are 32-bit
@@ -197,26 +243,30 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
   gdn::FwdParams q = p;
   cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&q.err), gdn::g_device_error);
   if (e != cudaSuccess) return cuda_fail(e, "locating the device error word");
+  if (check) {
+    e = gdn::launch_check_inputs(q, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the input check");
+  }
   return launch_pipeline(q, w, stream);
 }
 
 gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cudaStream_t stream) {
-  cudaError_t e = p.kda ? gdn::launch_kda_prep(p, w, stream) : gdn::launch_prep(p, w, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
-  if (w.blocks) {  // dk = dv = 128, gated delta rule: 128-token blocks
-    if (gdn::scan_out_fused(p)) {  // pair, scan and output work in one launch
-      e = gdn::launch_scan_out(p, w, stream, true);
-      if (e != cudaSuccess) return cuda_fail(e, "launching the block kernel");
-      return GDN_OK;
-    }
-    e = gdn::launch_pair(p, w, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the pair kernel");
-    e = gdn::launch_scan(p, w, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the scan kernel");
-    e = gdn::launch_out(p, w, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the output kernel");
+  if (p.tc_chain) {  // lookahead records, the tcgen05 chain
+    cudaError_t e = gdn::launch_prep_tc(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
+    e = gdn::launch_chain_tc(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the chain kernel");
     return GDN_OK;
   }
+  if (p.kda) {  // Kimi Delta Attention: its own prep, the mma.sync chain
+    cudaError_t e = gdn::launch_kda_prep(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the KDA prep kernel");
+    e = gdn::launch_chain(p, w, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the KDA chain kernel");
+    return GDN_OK;
+  }
+  cudaError_t e = gdn::launch_prep(p, w, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the prep kernel");
   e = gdn::launch_chain(p, w, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launching the chain kernel");
   return GDN_OK;
@@ -235,9 +285,24 @@ gdn_status fwd_bf16_pooled(const gdn::FwdParams& p, cudaStream_t st) {
   return s;
 }
 
-gdn_status run_step(const gdn::StepParams& p, bool f32, cudaStream_t st) {
+gdn_status run_step(const gdn::StepParams& p, bool f32, cudaStream_t st, bool check = false) {
   if (p.N == 0) return GDN_OK;
-  cudaError_t e = f32 ? gdn::launch_step_f32(p, st) : gdn::launch_step_bf16(p, st);
+  cudaError_t e;
+  if (check) {  // the step's gates: one token of N rows
+    gdn::FwdParams c{};
+    c.g = p.g;
+    c.beta = p.beta;
+    c.N = p.N;
+    c.T = 1;
+    c.Hv = p.Hv;
+    c.dk = p.dk;
+    c.kda = p.kda;
+    c.prologue = p.prologue;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&c.err), gdn::g_device_error);
+    if (e == cudaSuccess) e = gdn::launch_check_inputs(c, st);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the input check");
+  }
+  e = f32 ? gdn::launch_step_f32(p, st) : gdn::launch_step_bf16(p, st);
   return e == cudaSuccess ? GDN_OK : cuda_fail(e, "launching the decode step");
 }
 
@@ -248,13 +313,16 @@ extern "C" {
 gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream) {
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream) {
   gdn::FwdParams p;
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
-  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  s = apply_flags(flags, true, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                      (flags & GDN_FLAG_CHECK_INPUTS) != 0);
 }
 
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
@@ -266,7 +334,7 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int d
                 const_cast<void*>(A), nullptr, B, T, Hqk, Hv, dk, dv, chunk, 1.0f,
                 has_cu_seqlens ? &fake_cu : nullptr, 2, &p) != GDN_OK)
     return 0;
-  return gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+  return gdn::ws_bytes_any(p);
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -300,6 +368,22 @@ gdn_status gdn_recurrent_step(const void* q, const void* k, const void* v, const
   return run_step(p, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
+gdn_status gdn_recurrent_step_ex(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float* h, void* o, int N, int Hqk, int Hv,
+                                 int dk, int dv, float scale, unsigned flags,
+                                 gdn_stream_t stream) {
+  gdn::StepParams p;
+  gdn_status s = check_step(q, k, v, g, beta, h, o, N, Hqk, Hv, dk, dv, scale, &p);
+  if (s != GDN_OK) return s;
+  constexpr unsigned kStepFlags = GDN_FLAG_HEAD_MAP_MODULO | GDN_FLAG_CHECK_INPUTS;
+  if (flags & ~kStepFlags)
+    return fail(GDN_ERR_INVALID_ARG, "flag bits 0x%x do not apply to the decode step",
+                flags & ~kStepFlags);
+  p.head_map = (flags & GDN_FLAG_HEAD_MAP_MODULO) ? 1 : 0;
+  return run_step(p, false, reinterpret_cast<cudaStream_t>(stream),
+                  (flags & GDN_FLAG_CHECK_INPUTS) != 0);
+}
+
 gdn_status gdn_recurrent_step_f32(const float* q, const float* k, const float* v,
                                   const float* g, const float* beta, float* h, float* o, int N,
                                   int Hqk, int Hv, int dk, int dv, float scale,
@@ -315,7 +399,7 @@ gdn_status gdn_chunk_fwd_prologue_ex(const void* q, const void* k, const void* v
                                      const float* b, const float* A_log, const float* dt_bias,
                                      const float* h0, void* o, float* hT, int B, int T, int Hqk,
                                      int Hv, int dk, int dv, int chunk, float scale,
-                                     const int32_t* cu_seqlens, void* workspace,
+                                     const int32_t* cu_seqlens, unsigned flags, void* workspace,
                                      size_t workspace_bytes, gdn_stream_t stream) {
   gdn::FwdParams p;
   gdn_status s = check_fwd(q, k, v, a, b, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
@@ -323,10 +407,13 @@ gdn_status gdn_chunk_fwd_prologue_ex(const void* q, const void* k, const void* v
   if (s != GDN_OK) return s;
   if (!aligned(A_log, 4) || !aligned(dt_bias, 4))
     return fail(GDN_ERR_INVALID_ARG, "A_log and dt_bias must be 4-byte aligned");
+  s = apply_flags(flags, true, &p);
+  if (s != GDN_OK) return s;
   p.prologue = 1;
   p.A_log = A_log;
   p.dt_bias = dt_bias;
-  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                      (flags & GDN_FLAG_CHECK_INPUTS) != 0);
 }
 
 gdn_status gdn_chunk_fwd_prologue(const void* q, const void* k, const void* v, const float* a,
@@ -377,14 +464,17 @@ gdn_status ssd_chunk_fwd(const void* q, const void* k, const void* v, const floa
 gdn_status ssd_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream) {
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream) {
   gdn::FwdParams p;
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
+  s = apply_flags(flags, true, &p);
+  if (s != GDN_OK) return s;
   p.delta_rule = 0;
-  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                      (flags & GDN_FLAG_CHECK_INPUTS) != 0);
 }
 
 gdn_status ssd_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* g,
@@ -424,13 +514,16 @@ gdn_status ssd_recurrent_step_f32(const float* q, const float* k, const float* v
 gdn_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, const float* h0, void* o, float* hT, int B, int T,
                             int Hqk, int Hv, int dk, int dv, int chunk, float scale,
-                            const int32_t* cu_seqlens, void* workspace, size_t workspace_bytes,
-                            gdn_stream_t stream) {
+                            const int32_t* cu_seqlens, unsigned flags, void* workspace,
+                            size_t workspace_bytes, gdn_stream_t stream) {
   gdn::FwdParams p;
   gdn_status s = check_kda(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, &p);
   if (s != GDN_OK) return s;
-  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  s = apply_flags(flags, false, &p);
+  if (s != GDN_OK) return s;
+  return run_fwd_bf16(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                      (flags & GDN_FLAG_CHECK_INPUTS) != 0);
 }
 
 gdn_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -453,7 +546,7 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int d
                 const_cast<void*>(A), nullptr, B, T, Hqk, Hv, dk, dv, chunk, 1.0f,
                 has_cu_seqlens ? &fake_cu : nullptr, &p) != GDN_OK)
     return 0;
-  return gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+  return gdn::ws_bytes_any(p);
 }
 
 gdn_status kda_recurrent_step(const void* q, const void* k, const void* v, const float* g,
@@ -487,6 +580,14 @@ gdn_status gdn_device_status(gdn_stream_t stream) {
   if (word == gdn::kErrGateRange)
     return fail(GDN_ERR_INVALID_ARG,
                 "a KDA log-decay was below -10 or not a number: that call's result is not exact");
+  if (word == gdn::kErrOperandRange)
+    return fail(GDN_ERR_INVALID_ARG,
+                "an on-chip fp16 operand (V_new or the state) left fp16's range (|x| > 65504 or "
+                "not a number): that call's result is not exact");
+  if (word == gdn::kErrInput)
+    return fail(GDN_ERR_INVALID_ARG,
+                "input check: a gate outside its domain (g > 0, beta outside [0, 1], or not a "
+                "number) or cu_seqlens not ordered from 0 to T");
   if (word != 0u) return fail(GDN_ERR_TIMEOUT, "device error word 0x%x", word);
   return GDN_OK;
 }
@@ -497,12 +598,12 @@ gdn_status gdn_device_status(gdn_stream_t stream) {
 // A fixed workspace compiled into the library: the device keeps these bytes
 // from the moment the library's device code is first used until the process
 // exits, on every GPU it runs on.  Host code must not use the array's name as a
-// device address; the address is looked up once per device below.
+// device address; every call looks the address up for the current device
+// (cudaGetSymbolAddress allocates nothing), so nothing stale survives a device
+// reset.
 namespace {
 constexpr size_t kNoAllocWorkspaceBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
-std::mutex g_noalloc_mutex;
-void* g_noalloc_address[64] = {};  // per device ordinal, filled on first use
 }  // namespace
 
 extern "C" {
@@ -515,28 +616,15 @@ gdn_status gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
-  const size_t need = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);
+  const size_t need = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);  // the default path's records
   if (need > kNoAllocWorkspaceBytes)
     return fail(GDN_ERR_INVALID_ARG,
                 "these sizes need %zu bytes of workspace; the built-in workspace holds %zu "
                 "(use gdn_chunk_fwd_ex with a caller buffer)",
                 need, kNoAllocWorkspaceBytes);
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "querying the current device");
-  if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
   void* ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_address[dev]) {
-      e = cudaGetSymbolAddress(&g_noalloc_address[dev], g_noalloc_workspace);
-      if (e != cudaSuccess) {
-        g_noalloc_address[dev] = nullptr;
-        return cuda_fail(e, "locating the built-in workspace");
-      }
-    }
-    ws = g_noalloc_address[dev];
-  }
+  cudaError_t e = cudaGetSymbolAddress(&ws, g_noalloc_workspace);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the built-in workspace");
   return run_fwd_bf16(p, ws, kNoAllocWorkspaceBytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -553,6 +641,6 @@ const char* gdn_status_string(gdn_status s) {
 
 const char* gdn_last_error(void) { return t_last_error; }
 
-int gdn_abi_version(void) { return 1; }
+int gdn_abi_version(void) { return 2; }
 
 }  // extern "C"

@@ -238,6 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Per chunk: V_new (depth-4 accumulation chains: K split in two halves), one
   // barrier, the state update straight into the next H buffer, one barrier.
   // The A fragments of W and Kt are read before the state they multiply is ready.
+  // any fp16 copy of V_new or of the state that rounded to infinity (|x| past 65504)
+  // or is not a number: the fp16 operands are no longer exact and the call is reported
+  uint32_t f16bad = 0u;
   int c = 0;
   for (; c < n_chunks; ++c) {
     const unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
@@ -296,10 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       __half2float(Ut[swz<kC>(col + 1, r0)]));
         const float2 u1 = make_float2(__half2float(Ut[swz<kC>(col, r0 + 8)]),
                                       __half2float(Ut[swz<kC>(col + 1, r0 + 8)]));
-        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0, col)]) =
+        const uint32_t va =
             pack_f16(u0.x - wh[0][j][0] - wh[1][j][0], u0.y - wh[0][j][1] - wh[1][j][1]);
-        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0 + 8, col)]) =
+        const uint32_t vb =
             pack_f16(u1.x - wh[0][j][2] - wh[1][j][2], u1.y - wh[0][j][3] - wh[1][j][3]);
+        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0, col)]) = va;
+        *reinterpret_cast<uint32_t*>(&Vc[swz<DVT>(r0 + 8, col)]) = vb;
+        f16bad |= f16_inf_or_nan(va) | f16_inf_or_nan(vb);
       }
     }
     if (tid == 0) *s_cstop = *s_abort;
@@ -348,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int hr = 16 * (MTW * warp + mt) + gq, col = 8 * j + 2 * tq;
-        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr, col)]) =
-            pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
-        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr + 8, col)]) =
-            pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
+        const uint32_t ha = pack_f16(hacc[mt][j][0], hacc[mt][j][1]);
+        const uint32_t hb = pack_f16(hacc[mt][j][2], hacc[mt][j][3]);
+        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr, col)]) = ha;
+        *reinterpret_cast<uint32_t*>(&Hn[swz<DVT>(hr + 8, col)]) = hb;
+        f16bad |= f16_inf_or_nan(ha) | f16_inf_or_nan(hb);
       }
     named_sync(1, kComputeThreads);  // next state copy complete
     GDN_PHASE(23);  // state copy
   }
+  if (__any_sync(0xffffffffu, f16bad != 0u) && lane == 0) record_error(p.err, kErrOperandRange);
   if (tid == 0 && *s_abort) {  // a wait gave up: let the copies already issued land
     for (int cc = c + 1; cc < min(c + kStages, n_chunks); ++cc)
       mbar_wait(&full[cc % kStages], (cc / kStages) & 1, nullptr);
@@ -379,7 +387,6 @@ template <int DK, int DVT>
 cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream) {
   using Lo = ChainLayout<DK, DVT>;
   const long long grid = (long long)p.N * p.Hv * (p.dv / DVT);
-  if (!ws.qrec) return cudaErrorInvalidValue;  // the chain reads Q~ from the records
   if constexpr (DVT == 64) {  // 64-column tiles: only without the erase term (no W stage)
     using L64 = ChainLayout<DK, 64, true>;
     if (p.delta_rule || p.kda) return cudaErrorInvalidValue;

@@ -49,8 +49,23 @@ extern __device__ unsigned long long g_gdn_phase[64];  // defined in gdn_abi.cu;
 namespace gdn {
 
 // Device error word (read by gdn_device_status): a bounded wait gave up, or a KDA
-// log-decay lay outside the range the KDA forward is exact for.
-enum : unsigned { kErrNone = 0u, kErrWaitTimeout = 1u, kErrGateRange = 2u };
+// log-decay lay outside the range the KDA forward is exact for.  The first non-zero
+// code written stays until it is read.
+// kErrOperandRange: an on-chip fp16 operand (V_new or the state) left fp16's finite range,
+// so that call's result is not exact; kErrInput: the input check of an _ex call found a
+// gate outside its domain or an unordered cu_seqlens.
+enum : unsigned {
+  kErrNone = 0u,
+  kErrWaitTimeout = 1u,
+  kErrGateRange = 2u,
+  kErrOperandRange = 3u,
+  kErrInput = 4u
+};
+
+// Record `code` in the error word unless an earlier code is already there.
+__device__ __forceinline__ void record_error(unsigned* err, unsigned code) {
+  if (err) atomicCAS(err, kErrNone, code);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -103,7 +118,7 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, unsigned parity, 
         : "memory");
     if (done) return true;
     if (clock64() - t0 > limit) {
-      if (err) atomicExch(err, kErrWaitTimeout);
+      record_error(err, kErrWaitTimeout);
       return false;
     }
   }
@@ -275,6 +290,12 @@ __device__ __forceinline__ void bf16x8_to_f16x8_scaled(void* p, float scale) {
     h[i] = __floats2half2_rn(f.x * scale, f.y * scale);
   }
   *reinterpret_cast<uint4*>(p) = out;
+}
+
+// Non-zero if either fp16 half of `w` is an infinity or a NaN (exponent field all
+// ones): adding 1 to a full 5-bit exponent field carries into the half's sign bit.
+__device__ __forceinline__ uint32_t f16_inf_or_nan(uint32_t w) {
+  return ((w & 0x7c007c00u) + 0x04000400u) & 0x80008000u;
 }
 
 // C fragments of two adjacent n8 tiles -> the A fragment of one k16 step (fp16).

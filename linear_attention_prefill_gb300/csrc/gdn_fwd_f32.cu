@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_f32_kernel(const FwdParam
   const int dvt = blockIdx.x % n_dvt;
   const int hv = (blockIdx.x / n_dvt) % p.Hv;
   const int n = blockIdx.x / (n_dvt * p.Hv);
-  const int hq = hv / (p.Hv / p.Hqk);
+  const int hq = qk_head(hv, p.Hqk, p.Hv, p.head_map);
 
   long long t_begin, t_end;
   if (p.cu_seqlens) {

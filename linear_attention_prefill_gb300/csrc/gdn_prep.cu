@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
   const int t0 = (int)(t_seq + (long long)c * kC);  // row in the flattened [tokens, H d] maps
   const int L = (int)min((long long)kC, len - (long long)c * kC);
-  const int hq = hv / (p.Hv / p.Hqk);
+  const int hq = qk_head(hv, p.Hqk, p.Hv, p.head_map);
 
   // ---- setup: barriers, the K/Q (and a separate V) loads, tensor memory -----
   if (tid == 0) {
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       const unsigned char* src = sm + (ch >> 3) * 16384 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(Kt + swzb<kC>(r, ch * 8)) = scale_bf16x8_to_f16(src, s_e[r]);
     }
-    if (ws.qrec) {  // the output's left factor diag(scale gamma) Q (norm folded in), fp16
+    {  // the output's left factor diag(scale gamma) Q (norm folded in), fp16
       __half* Qt = ws.Qt(slot, hv, p.Hv);
       for (int i = tid; i < kC * kRowChunks; i += kThreads) {
         const int r = i / kRowChunks, ch = i % kRowChunks;

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
   const int tile = blockIdx.x % ntile;
   const int hv = (blockIdx.x / ntile) % p.Hv;
   const int n = blockIdx.x / (ntile * p.Hv);
-  const int hq = hv / (p.Hv / p.Hqk);
+  const int hq = qk_head(hv, p.Hqk, p.Hv, p.head_map);
   const TIn* q = static_cast<const TIn*>(p.q) + ((long long)n * p.Hqk + hq) * DK;
   const TIn* k = static_cast<const TIn*>(p.k) + ((long long)n * p.Hqk + hq) * DK;
   for (int i = tid; i < DK; i += kWarps * 32) {

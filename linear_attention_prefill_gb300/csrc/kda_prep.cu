@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
       p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
   const long long t0 = t_seq + (long long)c * kC;  // first token of the chunk
   const int L = (int)min((long long)kC, len - (long long)c * kC);
-  const int hq = hv / (p.Hv / p.Hqk);
+  const int hq = qk_head(hv, p.Hqk, p.Hv, p.head_map);
   const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k);
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
   const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v);
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
       x[i] = Gs[(32 * half + i) * kDK + ch];
       in_range = in_range && x[i] >= kMinGate;
     }
-    if (!in_range && p.err) atomicExch(p.err, kErrGateRange);
+    if (!in_range) record_error(p.err, kErrGateRange);
 #pragma unroll
     for (int i = 1; i < 32; ++i) x[i] += x[i - 1];
     if (half == 0) s_tot[ch] = x[31];

@@ -21,3 +21,26 @@ def cuda_lib():
         pytest.skip("no CUDA device")
     import linear_attention_prefill_gb300 as lap
     return lap
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Every parity comparison of the run: raw max-abs/RMS, the error after the bf16
+    storage allowance (the one the tolerance applies to) and the NMSE."""
+    try:
+        from helpers import RECORDS
+    except ImportError:
+        return
+    if not RECORDS:
+        return
+    tr = terminalreporter
+    tr.section("parity against the fp64 oracle")
+    tr.write_line(f"{'test':58s} {'qty':3s} {'raw maxabs/RMS':>14s} {'adjusted':>10s} {'NMSE':>10s}")
+    for name, qty, raw, adj, e in RECORDS:
+        tr.write_line(f"{name[:58]:58s} {qty:3s} {raw:14.3e} {adj:10.3e} {e:10.3e}")
+    worst = {}
+    for name, qty, raw, adj, e in RECORDS:
+        w = worst.setdefault(qty, [0.0, 0.0, 0.0])
+        w[0], w[1], w[2] = max(w[0], raw), max(w[1], adj), max(w[2], e)
+    for qty, (raw, adj, e) in worst.items():
+        tr.write_line(f"worst {qty}: raw {raw:.3e}, adjusted {adj:.3e}, NMSE {e:.3e} "
+                      f"over {sum(1 for r in RECORDS if r[1] == qty)} comparisons")

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.gdn_abi_version() == 1
+    assert lib.gdn_abi_version() == 2
     assert lib.gdn_status_string(0) == b"GDN_OK"
     assert lib.gdn_status_string(1) == b"GDN_ERR_INVALID_ARG"
     assert lib.gdn_status_string(2) == b"GDN_ERR_UNSUPPORTED"
@@ -130,30 +130,23 @@ def test_product_path_does_not_import_the_oracle():
 
 
 def test_workspace_size_formula(lib):
-    # chunk record: W^T [dk][64], Kt [64][dk], P [64][64], U^T [dv][64] (fp16), 132 fp32
-    # gate factors on a 128-byte line, then the fp16 Q~ tile [64][dk] (not with the block
-    # path, which reads q itself), padded to a 128-byte multiple
-    block_path = os.environ.get("GDN_BLOCK_PATH") == "1"
-
+    # gated delta rule record: W' [64][dk], X^T [64][64], U^T [dv][64] (fp16), 132 fp32 gate
+    # factors, then (on a 128-byte line) Q~ [64][dk], Kt [64][dk], P^T [64][64] (fp16),
+    # padded to a 128-byte multiple
     def rec(dk, dv):
-        raw = 2 * 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 132 * 4
-        gv_end = (raw + 127) // 128 * 128
-        blocks = block_path and dk == 128 and dv == 128
-        return gv_end if blocks else (gv_end + 64 * dk * 2 + 127) // 128 * 128
-    # block record (dk = dv = 128, block path on): N [dk][dk], B [dk][dv], H [dk][dv]
-    # (fp16) and 16 bytes for the block's gate, padded to a 128-byte multiple
-    blk = (128 * 128 * 2 * 3 + 16 + 127) // 128 * 128 if os.environ.get("GDN_BLOCK_PATH") == "1" else 0
-    # block path: per-block flags (pair done, two stored states) and a task counter
-    def flags(n_bslots, Hv):
-        return (n_bslots * Hv * 3 * 4 + 4 + 127) // 128 * 128 if blk else 0
-    # fixed-length rows: N * ceil(T/64) chunk slots and N * ceil(T/128) block slots, x Hv
-    assert lib.gdn_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == \
-        64 * 16 * rec(128, 128) + 32 * 16 * blk + flags(32, 16)
+        gv_end = 64 * dk * 2 + 64 * 64 * 2 + 64 * dv * 2 + 132 * 4
+        qt = (gv_end + 127) // 128 * 128
+        return (qt + 2 * 64 * dk * 2 + 64 * 64 * 2 + 127) // 128 * 128
+    # fixed-length rows: N * ceil(T/64) chunk slots, x Hv
+    assert lib.gdn_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == 64 * 16 * rec(128, 128)
     assert lib.gdn_chunk_fwd_workspace_size(2, 100, 1, 4, 128, 64, 64, 0) == 2 * 2 * 4 * rec(128, 64)
-    # packed rows: floor(T/64) + N + 1 chunk slots, floor(T/128) + N + 1 block slots
-    nb = 9849 // 128 + 9
+    # packed rows: floor(T/64) + N + 1 chunk slots
     assert lib.gdn_chunk_fwd_workspace_size(8, 9849, 16, 32, 128, 128, 64, 1) == \
-        (9849 // 64 + 9) * 32 * rec(128, 128) + nb * 32 * blk + flags(nb, 32)
+        (9849 // 64 + 9) * 32 * rec(128, 128)
+    # Kimi Delta Attention record: W^T [dk][64], Kt [64][dk], P [64][64], U^T [dv][64], gates,
+    # then Q~ [64][dk] on a 128-byte line
+    kda = (2 * 64 * 128 * 2 + 64 * 64 * 2 + 64 * 128 * 2 + 132 * 4 + 127) // 128 * 128 + 64 * 128 * 2
+    assert lib.kda_chunk_fwd_workspace_size(1, 4096, 16, 16, 128, 128, 64, 0) == 64 * 16 * kda
     # rejected sizes give 0
     assert lib.gdn_chunk_fwd_workspace_size(1, 64, 3, 4, 128, 128, 64, 0) == 0
     assert lib.gdn_chunk_fwd_workspace_size(1, 64, 1, 1, 96, 128, 64, 0) == 0
@@ -162,10 +155,31 @@ def test_workspace_size_formula(lib):
 def test_ex_rejects_small_or_misaligned_workspace(lib):
     need = lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
     args = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
-    assert lib.gdn_chunk_fwd_ex(*args, None, need, None) == 1
-    assert lib.gdn_chunk_fwd_ex(*args, A, need - 1, None) == 1
-    assert lib.gdn_chunk_fwd_ex(*args, A + 16, need, None) == 1
-    assert b"workspace" in lib.gdn_last_error()
+    # the size function covers every flag; a call checks what its own records need
+    for flags in (0, 1, 2, 4, 7):
+        assert lib.gdn_chunk_fwd_ex(*args, flags, None, need, None) == 1
+        assert lib.gdn_chunk_fwd_ex(*args, flags, A, need // 2, None) == 1
+        assert lib.gdn_chunk_fwd_ex(*args, flags, A + 16, need, None) == 1
+        assert b"workspace" in lib.gdn_last_error()
+    assert lib.gdn_chunk_fwd_ex(*args, 4, A, need - 1, None) == 1  # the larger records
+
+
+def test_ex_rejects_unknown_flags(lib):
+    need = lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
+    args = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
+    assert lib.gdn_chunk_fwd_ex(*args, 8, A, need, None) == 1
+    assert b"flag" in lib.gdn_last_error()
+    # the decode step takes the head map and the input check, not the chain choice
+    sargs = (A, A, A, A, A, A, A, 1, 1, 2, 128, 128, 0.088)
+    assert lib.gdn_recurrent_step_ex(*sargs, 4, None) == 1
+    assert lib.gdn_recurrent_step_ex(*sargs, 16, None) == 1
+    assert lib.gdn_recurrent_step_ex(A, A, A, A, A, None, A, 1, 1, 2, 128, 128, 0.088, 1,
+                                     None) == 1  # NULL state: the step's own checks run
+    # KDA has no tensor-memory chain
+    kargs = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
+    kneed = lib.kda_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
+    assert lib.kda_chunk_fwd_ex(*kargs, 4, A, kneed, None) == 2
+    assert lib.ssd_chunk_fwd_ex(*kargs, 8, A, need, None) == 1
 
 
 @pytest.mark.parametrize("case,status", [

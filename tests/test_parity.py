@@ -12,6 +12,7 @@ import pytest
 import torch
 
 from helpers import TOL, check_heads, rel_err, to_np
+from oracle import gdn_recurrent
 from linear_attention_prefill_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -116,8 +117,20 @@ def test_split_resume_matches_one_call(cuda_lib, dtype):
          for k_, v_ in x.items()}
     b["h0"] = ha
     ob, hb = run(cuda_lib, b)
-    assert torch.equal(torch.cat([oa, ob], dim=1), o)
-    assert torch.equal(hb, hT)
+    if dtype == "f32":  # one fused launch: both sides take the same roundings
+        assert torch.equal(torch.cat([oa, ob], dim=1), o)
+        assert torch.equal(hb, hT)
+    else:
+        # The bf16 chain reads the state of chunk c through the previous chunk's operands
+        # (W'(c) h(c-1) + X(c) V_new(c-1)); a resumed call reads its first chunk's state
+        # directly from h0, so the two round differently: the split is checked within the
+        # tolerance, against the one call and against the oracle.
+        ref_o, ref_h = gdn_recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], x["h0"])
+        split_o = to_np(torch.cat([oa, ob], dim=1))
+        assert rel_err(split_o, to_np(o)) < TOL[dtype]
+        assert rel_err(to_np(hb), to_np(hT)) < TOL[dtype]
+        assert rel_err(split_o, ref_o, out_dtype=dtype) < TOL[dtype]
+        assert rel_err(to_np(hb), ref_h) < TOL[dtype]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -196,6 +209,17 @@ def test_workload(cuda_lib, name):
     print(f"{name}: err_o={eo:.3e} err_h={eh:.3e}")
     # properties that hold at any size: finite everywhere
     assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["layer_16h_4k", "gqa_32v_8k_state"])
+def test_workload_every_head(cuda_lib, name):
+    """Every v head of the headline layer and of the GQA 8K layer against the oracle, as
+    bench.py launches them (no sampling of heads)."""
+    w = WORKLOADS[name]
+    x = make_inputs(w, device="cuda")
+    o, hT = run(cuda_lib, x, chunk=w.chunk)
+    check_heads(x, o, hT, heads=range(w.Hv), dtype=w.dtype)
 
 
 def test_allocating_entry_point_matches_workspace_entry_point(cuda_lib):
