@@ -12,6 +12,12 @@ every rank runs its own batch (weak scaling, no collective on the data path).
 
 Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.
+
+CPU baselines (rank 0, N = 1, outside every timed GPU region): the fp64 oracle over
+v heads in a spawn-started process pool on the host cores (``cpu_baseline``), which
+also checks the GPU output of the timed calls on that sample (``parity``), and the
+fp32 per-token recurrence in C with OpenMP on all host cores and on one core
+(``cpu_baseline.fp32_recurrence``).
 """
 from __future__ import annotations
 
@@ -23,7 +29,6 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import csv
-import hashlib
 import io
 import json
 import statistics
@@ -49,18 +54,20 @@ L2_FLUSH_BYTES = 320 * 2 ** 20
 # prep kernel, then the chunk-serial chain kernel that also writes o); the fp32 path
 # is one fused launch.  The roofline block times the call, and the launch list in
 # profiles/ gives each kernel's share.
-KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_tc_kernel)"
-KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_tc_kernel, no erase term)",
+KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
+KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
                 "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
                 "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
-                                "gdn_chain_tc_kernel)",
+                                "gdn_chain_kernel)",
                 "f32": "gdn_chunk_fwd_f32 (gdn_fwd_f32_kernel)",
                 "ssd_f32": "ssd_chunk_fwd_f32 (gdn_fwd_f32_kernel, no erase term)"}
 
 
-def kernel_name(w) -> str:
+def kernel_name(w, tc_chain=False) -> str:
     if w.dtype == "f32":
         return KERNEL_NAMES["ssd_f32" if w.op == "ssd" else "f32"]
+    if tc_chain:
+        return f"{w.op}_chunk_fwd with GDN_FLAG_TC_CHAIN (gdn_prep_tc_kernel + gdn_chain_tc_kernel)"
     return KERNEL_NAMES.get("gdn_prologue" if w.prologue else w.op, KERNEL_NAME)
 
 
@@ -68,17 +75,6 @@ def launches_per_call(w) -> int:
     """Kernel launches of one forward call: the fp32 path is one fused launch; the bf16
     path a prep launch and a chain launch."""
     return 1 if w.dtype == "f32" else 2
-
-
-def kernel_source_hash() -> str:
-    csrc = os.path.join(ROOT, "linear_attention_prefill_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
-    return h.hexdigest()[:16]
 
 
 def measured_traffic(workload: str):
@@ -90,7 +86,7 @@ def measured_traffic(workload: str):
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("kernel_source_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_source_hash") != roofline.kernel_source_hash():
         return None
     return rec.get("dram_bytes_per_call")
 
@@ -152,26 +148,35 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def run_decode(lap, w, dev, steps=200):
-    """µs per decode step on this workload's state shape, plain and as a CUDA graph."""
+def run_decode(lap, w, dev, steps=1000):
+    """Decode on workload ``w``'s state shape, continuing from its prefill: one forward
+    gives hT, then ``steps`` one-token steps update it in place - timed as separate
+    launches and as one CUDA graph of all the steps.  Returns µs per step and the HBM
+    bandwidth that implies (state read + written, the token's q, k, v, g, beta and o)."""
     stepfn = {"ssd": lap.ssd_recurrent_step, "kda": lap.kda_recurrent_step}.get(
         w.op, lap.gdn_recurrent_step)
+    fwd = {"ssd": lap.ssd_chunk_fwd, "kda": lap.kda_chunk_fwd}.get(w.op, lap.gdn_chunk_fwd)
+    x = make_inputs(w, device=dev)
+    _, h = fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], chunk=w.chunk,
+               scale=w.scale, cu_seqlens=x["cu_seqlens"])
+    del x
+    toks = [make_decode_inputs(w, s, device=dev) for s in range(steps)]
+    d = {n: torch.stack([t[n] for t in toks]) for n in ("q", "k", "v", "g", "beta")}
+    del toks
     N, Hv = w.n_seqs, w.Hv
-    h = torch.randn((N, Hv, w.dk, w.dv), device=dev) * 0.1
-    d = make_decode_inputs(w, 0, device=dev)
-    o = torch.empty((N, Hv, w.dv), dtype=d["q"].dtype, device=dev)
+    o = torch.empty((steps, N, Hv, w.dv), dtype=d["q"].dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def one():
-        stepfn(d["q"], d["k"], d["v"], d["g"], d["beta"], h, o)
+    def run_all():
+        for s in range(steps):
+            stepfn(d["q"][s], d["k"][s], d["v"][s], d["g"][s], d["beta"][s], h, o[s],
+                   scale=w.scale)
 
-    for _ in range(10):
-        one()
+    run_all()  # warm-up (and the state keeps evolving from the prefill's)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        one()
+    run_all()
     b.record(stream)
     torch.cuda.synchronize()
     plain = a.elapsed_time(b) * 1e3 / steps
@@ -179,29 +184,30 @@ def run_decode(lap, w, dev, steps=200):
     try:
         s = torch.cuda.Stream(dev)
         s.wait_stream(stream)
-        with torch.cuda.stream(s):
-            one()
-        stream.wait_stream(s)
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(100):
-                one()
+        with torch.cuda.graph(g, stream=s):
+            run_all()
+        stream.wait_stream(s)
         g.replay()
         torch.cuda.synchronize()
         a.record(stream)
-        for _ in range(steps // 100):
-            g.replay()
+        g.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        graph_us = a.elapsed_time(b) * 1e3 / (100 * (steps // 100))
+        graph_us = a.elapsed_time(b) * 1e3 / steps
     except RuntimeError:
         graph_us = None
     nbytes = roofline.decode_bytes(N, w.Hqk, Hv, w.dk, w.dv, 2 if w.dtype == "bf16" else 4,
                                    gate_per_channel=w.op == "kda")
-    return {"us_per_step": round(plain, 3),
-            "us_per_step_cuda_graph": None if graph_us is None else round(graph_us, 3),
-            "bytes_per_step": nbytes,
-            "achieved_gbs_graph": None if graph_us is None else round(nbytes / graph_us / 1e3, 1)}
+    peaks, _ = roofline.load_peaks()
+    out = {"workload": w.name, "from": "the prefill's final state", "steps": steps,
+           "us_per_step": round(plain, 3),
+           "us_per_step_cuda_graph": None if graph_us is None else round(graph_us, 3),
+           "bytes_per_step": nbytes,
+           "achieved_gbs_graph": None if graph_us is None else round(nbytes / graph_us / 1e3, 1)}
+    if graph_us is not None:
+        out["hbm_frac_graph"] = round(nbytes / graph_us / 1e3 / peaks["hbm_gbs"], 4)
+    return out
 
 
 def oracle_tokens_per_s(w, x_cpu, budget_s):
@@ -228,6 +234,116 @@ def oracle_tokens_per_s(w, x_cpu, budget_s):
     return n_tok / dt, f"first {n_tok} tokens of sequence 0, all {H} v heads, fp64 numpy, 1 thread", dt
 
 
+def _oracle_head(args):
+    """One v head of the fp64 oracle (a spawn-started pool worker).  The inputs and the
+    output live in shared memory blocks named in ``args``; returns the seconds taken."""
+    from multiprocessing import shared_memory
+    op, names, shapes, hv, hq, n_tok, scale, has_h0 = args
+    blocks = {n: shared_memory.SharedMemory(name=names[n]) for n in names}
+    try:
+        arr = {n: np.ndarray(shapes[n], dtype=np.float64, buffer=blocks[n].buf) for n in names}
+        import oracle
+        fwd = {"ssd": oracle.ssd_recurrent, "kda": oracle.kda_recurrent}.get(op,
+                                                                           oracle.gdn_recurrent)
+        sl = slice(0, n_tok)
+        t = time.perf_counter()
+        o, _ = fwd(arr["q"][:, sl, hq:hq + 1], arr["k"][:, sl, hq:hq + 1],
+                   arr["v"][:, sl, hv:hv + 1], arr["g"][:, sl, hv:hv + 1],
+                   arr["beta"][:, sl, hv:hv + 1], scale,
+                   arr["h0"][:, hv:hv + 1] if has_h0 else None)
+        dt = time.perf_counter() - t
+        arr["o"][:n_tok, hv] = o[0, :, 0]
+        return dt
+    finally:
+        for b in blocks.values():
+            b.close()
+
+
+def oracle_pool_rate(w, xc, budget_s, workers):
+    """The fp64 oracle over the first n tokens of every v head of row 0, one head per task
+    in a pool of ``workers`` spawn-started processes (inputs and output in shared memory),
+    n sized so the pool's wall time is about ``budget_s``.  Returns (tokens/s of the layer,
+    sample text, wall s, o [n, Hv, dv])."""
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    T = w.seqlens[0]
+    src = {n: xc[n][:1, :T].float().numpy() for n in ("q", "k", "v", "g", "beta")}
+    if xc["h0"] is not None:
+        src["h0"] = xc["h0"][:1].numpy()
+    src["o"] = np.zeros((T, w.Hv, w.dv))
+    blocks, names, shapes = {}, {}, {}
+    try:
+        for n, a in src.items():
+            b = shared_memory.SharedMemory(create=True, size=max(8, a.size * 8))
+            np.ndarray(a.shape, dtype=np.float64, buffer=b.buf)[...] = a
+            blocks[n], names[n], shapes[n] = b, b.name, a.shape
+        rep = w.Hv // w.Hqk
+
+        def tasks(n_tok):
+            return [(w.op, names, shapes, hv, hv // rep, n_tok, w.scale, "h0" in src)
+                    for hv in range(w.Hv)]
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers) as pool:
+            probe = min(T, 64)
+            per_tok = max(pool.map(_oracle_head, tasks(probe)[:workers])) / probe
+            waves = -(-w.Hv // workers)
+            n_tok = int(max(probe, min(T, budget_s / (per_tok * waves))))
+            t = time.perf_counter()
+            pool.map(_oracle_head, tasks(n_tok))
+            wall = time.perf_counter() - t
+        o = np.ndarray(shapes["o"], dtype=np.float64, buffer=blocks["o"].buf)[:n_tok].copy()
+    finally:
+        for b in blocks.values():
+            b.close()
+            b.unlink()
+    sample = (f"first {n_tok} tokens of sequence 0, all {w.Hv} v heads, fp64 numpy, "
+              f"one head per task, {workers} processes")
+    return n_tok / wall, sample, wall, o
+
+
+def parity_sample(o_gpu, o_ref, dtype):
+    """max |x - ref| / RMS(ref) raw and after half a bf16 ulp of |ref| per element, and the
+    NMSE, of the GPU output against the oracle on the sampled tokens."""
+    x = o_gpu.astype(np.float64)
+    d = np.abs(x - o_ref)
+    rms = float(np.sqrt(np.mean(o_ref ** 2))) or 1.0
+    adj = d
+    if dtype == "bf16":
+        a = np.abs(o_ref)
+        half_ulp = np.where(a > 0, np.exp2(np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
+        adj = np.maximum(d - half_ulp, 0.0)
+    return {"max_abs_over_rms": float(d.max() / rms), "max_abs_over_rms_adjusted":
+            float(adj.max() / rms), "nmse": float(np.sum(d ** 2) / np.sum(o_ref ** 2)),
+            "tolerance": 2e-2 if dtype == "bf16" else 1e-4}
+
+
+def fp32_recurrence_baseline(w, xc, budget_s):
+    """The fp32 per-token recurrence (C, OpenMP) on all host cores and on one core; tokens/s
+    of the layer.  All cores run row 0 whole when that fits the budget, else a prefix."""
+    import cpu_baseline as cb
+    cores = cb.host_cores()
+    x = {n: (None if xc[n] is None else xc[n].float().numpy()) for n in
+         ("q", "k", "v", "g", "beta", "h0")}
+    x["cu_seqlens"] = None
+    T = w.seqlens[0]
+    probe = {n: (None if a is None else a[:, :min(T, 256)]) if n != "h0" else a for n, a in x.items()}
+    probe["cu_seqlens"] = None
+    t = cb.time_recurrence_f32(probe, w.scale, cores)
+    n_tok = int(max(64, min(T, budget_s / max(t / min(T, 256), 1e-9))))
+    xs = {n: (None if a is None else a[:, :n_tok]) if n not in ("h0", "cu_seqlens") else a
+          for n, a in x.items()}
+    t_all = cb.time_recurrence_f32(xs, w.scale, cores, reps=3)
+    # one core: one q/k head and the v heads that read it, over the same tokens; the
+    # layer's rate on one core counts all Hqk such groups
+    t_group = cb.time_recurrence_f32(xs, w.scale, 1, groups=1, reps=2)
+    return {"value": n_tok / t_all, "unit": UNIT, "cores": cores, "kind": "fp32 per-token recurrence "
+            "(C, OpenMP over (sequence, v head) chains)", "cpu_model": cb.cpu_model(),
+            "sample": f"first {n_tok} tokens of sequence 0, all {w.Hv} v heads",
+            "one_core": {"value": n_tok / (t_group * w.Hqk), "unit": UNIT, "cores": 1,
+                         "sample": f"the same tokens, one q/k head group of {w.Hv // w.Hqk} v "
+                                   f"heads, timed and scaled to the layer's {w.Hqk} groups"}}
+
+
 def cpu_inputs(w, x):
     """The same tensors on the host (first sequence row only) for the oracle legs."""
     out = {}
@@ -237,25 +353,44 @@ def cpu_inputs(w, x):
     return out
 
 
+def oracle_workers(w):
+    """Processes for the oracle pool: the host's cores, at most one per v head."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(n, w.Hv))
+
+
 def bench_reference(args, w, rank, world):
     if rank != 0:
         return
     x = make_inputs(w, device="cpu")
     xc = cpu_inputs(w, x)
-    for _ in range(args.warmup):
-        oracle_tokens_per_s(w, xc, 0.05)
+    workers = oracle_workers(w)
     times, rates = [], []
     sample = ""
-    for _ in range(args.steps):
-        r, sample, dt = oracle_tokens_per_s(w, xc, args.ref_step_s)
-        rates.append(r)
-        times.append(dt)
+    if w.prologue:
+        for _ in range(args.warmup):
+            oracle_tokens_per_s(w, xc, 0.05)
+        for _ in range(args.steps):
+            r, sample, dt = oracle_tokens_per_s(w, xc, args.ref_step_s)
+            rates.append(r)
+            times.append(dt)
+        workers = 1
+    else:
+        for _ in range(args.warmup):
+            oracle_pool_rate(w, xc, 0.05, workers)
+        for _ in range(args.steps):
+            r, sample, dt, _ = oracle_pool_rate(w, xc, args.ref_step_s, workers)
+            rates.append(r)
+            times.append(dt)
     value = len(rates) / sum(1.0 / r for r in rates)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w, 1), "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -276,10 +411,11 @@ def bench_cuda(args, w, rank, world, local_rank):
     if w.prologue:  # raw q, k and gate inputs through the fused prologue
         def fwd(q, k, v, a, b, h0, o, hT, **kw):
             return lap.gdn_chunk_fwd_prologue(q, k, v, a, b, None, None, h0, o, hT, **kw)
+    extra = {"tc_chain": True} if args.tc_chain else {}
 
     def step():
         fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
-            scale=w.scale, cu_seqlens=x["cu_seqlens"], stream=stream)
+            scale=w.scale, cu_seqlens=x["cu_seqlens"], stream=stream, **extra)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -330,7 +466,7 @@ def bench_cuda(args, w, rank, world, local_rank):
     e2e_ms, e2e_tok = reduce_timing(e2e_s * 1e3, float(w.T_total * e2e_steps))
     e2e_value = e2e_tok / (e2e_ms / 1e3)
 
-    decode = run_decode(lap, w, dev) if args.decode else None
+    decode = run_decode(lap, WORKLOADS[args.decode_workload], dev) if args.decode else None
 
     if rank != 0:
         return
@@ -342,11 +478,13 @@ def bench_cuda(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, world),
+        "config": config_of(w, world, {"chain": "tcgen05 (state in tensor memory)"
+                                       if args.tc_chain else "mma.sync (dv tiles)"}),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": measured_traffic(w.name), "peak_source": src,
-                     "kernel": kernel_name(w),
+                     "traffic": measured_traffic(w.name + (":tc" if args.tc_chain else "")),
+                     "peak_source": src,
+                     "kernel": kernel_name(w, args.tc_chain),
                      "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],
                      "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),
@@ -362,9 +500,22 @@ def bench_cuda(args, w, rank, world, local_rank):
         line["decode"] = decode
     if world == 1 and args.cpu_baseline:
         xc = cpu_inputs(w, x)
-        rate, sample, _ = oracle_tokens_per_s(w, xc, args.cpu_baseline_s)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+        o_cpu = o[:1].float().cpu().numpy()
+        if w.prologue:
+            rate, sample, _ = oracle_tokens_per_s(w, xc, args.cpu_baseline_s)
+            cores = 1
+            par = None
+        else:
+            cores = oracle_workers(w)
+            rate, sample, _, o_ref = oracle_pool_rate(w, xc, args.cpu_baseline_s, cores)
+            par = parity_sample(o_cpu[0, :o_ref.shape[0]], o_ref, w.dtype)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
+        if w.op == "gdn" and not w.prologue:
+            line["cpu_baseline"]["fp32_recurrence"] = fp32_recurrence_baseline(
+                w, xc, args.cpu_baseline_s / 2)
+        if par is not None:
+            line["parity"] = dict(par, sample=sample)
     print(json.dumps(line), flush=True)
 
 
@@ -379,6 +530,10 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=0.5)
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--tc-chain", action="store_true",
+                    help="run the chunk-serial operators on the tensor-memory chain")
+    ap.add_argument("--decode-workload", default="long_64k_weak", choices=sorted(WORKLOADS),
+                    help="state shape of the decode measurement (continues from its prefill)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -69,8 +69,10 @@ enum {
    * fp32 state resident in tensor memory: one CTA per (sequence, v head), the
    * one-chunk lookahead form of the state read (the forwards' _ex entry points;
    * KDA returns GDN_ERR_UNSUPPORTED).  Same function and tolerances; uses one SM
-   * per chain where the default uses dv / 16 (or 32), so it pays off when many
-   * chains share the GPU. */
+   * per chain where the dv-tile chain uses dv / 16 (or / 32), so it pays off when
+   * many chains share the GPU.  Without the flag every forward picks it by
+   * itself when the dv-tile chain would need several times more waves of CTAs
+   * over the SMs (e.g. 8 packed sequences x 32 v heads). */
   GDN_FLAG_TC_CHAIN = 4u
 };
 

@@ -236,11 +236,12 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
   if ((p.cu_seqlens ? 1ll : (long long)p.N) * p.T > 0x7fffffffll)
     return fail(GDN_ERR_UNSUPPORTED, "%lld tokens: the bf16 path takes at most 2^31 - 1",
                 (p.cu_seqlens ? 1ll : (long long)p.N) * p.T);
-  const gdn::WsLayout w = gdn::ws_layout(p, ws);
+  gdn::FwdParams q = p;
+  if (!q.tc_chain && gdn::tc_chain_pays(q)) q.tc_chain = 1;  // many chains: one CTA each
+  const gdn::WsLayout w = gdn::ws_layout(q, ws);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % 256) != 0 || ws_size < gdn::ws_bytes(w, p.Hv))
     return fail(GDN_ERR_INVALID_ARG, "workspace %p of %zu bytes: need %zu bytes, 256-byte aligned",
                 ws, ws_size, gdn::ws_bytes(w, p.Hv));
-  gdn::FwdParams q = p;
   cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&q.err), gdn::g_device_error);
   if (e != cudaSuccess) return cuda_fail(e, "locating the device error word");
   if (check) {
@@ -275,7 +276,7 @@ gdn_status launch_pipeline(const gdn::FwdParams& p, const gdn::WsLayout& w, cuda
 // bf16 forward on a workspace taken from the stream-ordered pool and given back after.
 gdn_status fwd_bf16_pooled(const gdn::FwdParams& p, cudaStream_t st) {
   if (p.N == 0 || (!p.cu_seqlens && p.T == 0)) return run_fwd_bf16(p, nullptr, 0, st);
-  const size_t bytes = gdn::ws_bytes(gdn::ws_layout(p, nullptr), p.Hv);
+  const size_t bytes = gdn::ws_bytes_any(p);
   void* ws = nullptr;
   cudaError_t e = cudaMallocAsync(&ws, bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "allocating the workspace");
@@ -616,7 +617,7 @@ gdn_status gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
   gdn_status s = check_fwd(q, k, v, g, beta, h0, o, hT, B, T, Hqk, Hv, dk, dv, chunk, scale,
                            cu_seqlens, 2, &p);
   if (s != GDN_OK) return s;
-  const size_t need = gdn::ws_bytes(gdn::ws_layout(p, nullptr), Hv);  // the default path's records
+  const size_t need = gdn::ws_bytes_any(p);
   if (need > kNoAllocWorkspaceBytes)
     return fail(GDN_ERR_INVALID_ARG,
                 "these sizes need %zu bytes of workspace; the built-in workspace holds %zu "

@@ -160,6 +160,19 @@ inline int dv_tile(const FwdParams& p) {
   return 32;
 }
 
+// Which chain runs when the caller does not ask for the tcgen05 one: the mma.sync
+// chain walks one CTA per (chain, dv tile) at ~0.95 us a chunk, the tcgen05 chain one
+// CTA per chain at ~2.2 us a chunk (measured on GB300), so the tcgen05 chain is taken
+// when the mma.sync chain would need that many more waves of CTAs over the SMs.  KDA
+// records exist for the mma.sync chain only.
+inline bool tc_chain_pays(const FwdParams& p) {
+  if (p.kda) return false;
+  const long long chains = (long long)p.N * p.Hv;
+  const long long tiles = p.dv / dv_tile(p);
+  const long long waves_mma = (chains * tiles + 151) / 152, waves_tc = (chains + 151) / 152;
+  return 22 * waves_tc < 95 * waves_mma / 10;
+}
+
 // Layout for one call (sizes validated); base may be null when only sizing.
 inline WsLayout ws_layout(const FwdParams& p, void* base) {
   WsLayout w;

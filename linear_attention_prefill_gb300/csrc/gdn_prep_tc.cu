@@ -142,7 +142,7 @@ __device__ __forceinline__ float decay_of(const FwdParams& p, float raw, float a
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 3)
-    gdn_prep_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq,
+    gdn_prep_tc_kernel(const FwdParams p, const WsLayout ws, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using Lo = PrepLayout<DK, DV>;
   extern __shared__ unsigned char smem_raw[];
@@ -675,15 +675,15 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
       !make_tensor_map_bf16(&mk, p.k, rows, (long long)p.Hqk * DK) ||
       !make_tensor_map_bf16(&mv, p.v, rows, (long long)p.Hv * DV))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gdn_prep_kernel<DK, DV>,
+  cudaError_t e = cudaFuncSetAttribute(gdn_prep_tc_kernel<DK, DV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gdn_prep_kernel<DK, DV>,
+    e = cudaFuncSetAttribute(gdn_prep_tc_kernel<DK, DV>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   const long long grid = ws.n_slots * p.Hv;
-  gdn_prep_kernel<DK, DV><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq, mk, mv);
+  gdn_prep_tc_kernel<DK, DV><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mq, mk, mv);
   return cudaGetLastError();
 }
 

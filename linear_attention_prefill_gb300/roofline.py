@@ -105,3 +105,91 @@ def workload_model(w, peaks):
     t_fl = f / tc
     return dict(bytes=b, flops=f, t_hbm=t_hbm, t_flop=t_fl, t_roof=max(t_hbm, t_fl),
                 bound="hbm" if t_hbm >= t_fl else ("alu" if w.dtype == "f32" else "tensor"))
+
+
+# ---- measured DRAM traffic (ncu) ---------------------------------------------------
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash() -> str:
+    """Hash of every CUDA source of the library: a traffic figure is shown only for
+    the exact sources it was measured on."""
+    import hashlib
+    csrc = os.path.join(ROOT, "linear_attention_prefill_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_ncu_csv(path, launches_per_call):
+    """DRAM bytes per forward call from an ncu --csv launch list that holds
+    dram__bytes_read.sum and dram__bytes_write.sum for whole calls of
+    ``launches_per_call`` consecutive launches; returns (bytes per call, per-kernel
+    read/write means)."""
+    import csv
+    rows = []
+    with open(path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        rows.append(r)
+    launches = {}
+    for r in rows:
+        d = launches.setdefault(int(r["ID"]), {"kernel": r["Kernel Name"]})
+        if r["Metric Name"] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            d[r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
+    ids = sorted(launches)
+    calls = len(ids) // launches_per_call
+    if calls == 0:
+        raise ValueError(f"{path}: fewer than {launches_per_call} launches")
+    per_call = []
+    kernels = {}
+    for c in range(calls):
+        tot = 0.0
+        for i in ids[c * launches_per_call:(c + 1) * launches_per_call]:
+            d = launches[i]
+            rd, wr = d.get("dram__bytes_read.sum", 0.0), d.get("dram__bytes_write.sum", 0.0)
+            tot += rd + wr
+            k = kernels.setdefault(d["kernel"].split("(")[0], [0.0, 0.0, 0])
+            k[0] += rd
+            k[1] += wr
+            k[2] += 1
+        per_call.append(tot)
+    kern = {k: {"dram_read": int(v[0] / v[2]), "dram_write": int(v[1] / v[2])}
+            for k, v in kernels.items()}
+    return int(sum(per_call) / len(per_call)), kern
+
+
+def write_traffic(csv_path, workload, kernel, launches_per_call, source):
+    """Record a workload's measured DRAM bytes per call in profiles/traffic.json, stamped
+    with the current kernel source hash."""
+    per_call, kern = traffic_from_ncu_csv(csv_path, launches_per_call)
+    try:
+        with open(TRAFFIC_JSON) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data[workload] = {"kernel": kernel, "kernel_source_hash": kernel_source_hash(),
+                      "dram_bytes_per_call": per_call, "kernels": kern,
+                      "cache": "cold: ncu flushes L2 before each profiled launch; mean over "
+                               "the profiled calls", "source": source}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(data, f, indent=1)
+    return per_call
+
+
+if __name__ == "__main__":
+    import argparse
+    ap = argparse.ArgumentParser(description="record measured DRAM traffic per forward call "
+                                             "from an ncu --csv launch list")
+    ap.add_argument("csv")
+    ap.add_argument("--workload", required=True)
+    ap.add_argument("--kernel", required=True, help="what one call launches")
+    ap.add_argument("--launches-per-call", type=int, default=2)
+    ap.add_argument("--source", default="", help="the profiles/ summary of the capture")
+    a = ap.parse_args()
+    print(write_traffic(a.csv, a.workload, a.kernel, a.launches_per_call, a.source))
