@@ -63,12 +63,26 @@ KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no er
                 "ssd_f32": "ssd_chunk_fwd_f32 (gdn_fwd_f32_kernel, no erase term)"}
 
 
-def kernel_name(w, tc_chain=False) -> str:
+def kernel_name(w, chain="dv_tile") -> str:
     if w.dtype == "f32":
         return KERNEL_NAMES["ssd_f32" if w.op == "ssd" else "f32"]
-    if tc_chain:
-        return f"{w.op}_chunk_fwd with GDN_FLAG_TC_CHAIN (gdn_prep_tc_kernel + gdn_chain_tc_kernel)"
+    if chain == "tc":
+        fn = "gdn_chunk_fwd_prologue" if w.prologue else f"{w.op}_chunk_fwd"
+        return f"{fn} (gdn_prep_tc_kernel + gdn_chain_tc_kernel)"
     return KERNEL_NAMES.get("gdn_prologue" if w.prologue else w.op, KERNEL_NAME)
+
+
+def chain_of(lap, w, choice) -> str:
+    """The chain kernel the bf16 forward of ``w`` runs ("tc" or "dv_tile"; "-" for fp32)
+    under --chain ``choice``."""
+    if w.dtype == "f32":
+        return "-"
+    forced = {"auto": None, "tc": True, "dv_tile": False}[choice]
+    return lap.chain_kind(w.n_seqs, w.Hv, w.dk, w.dv, w.op, forced)
+
+
+CHAIN_LABEL = {"tc": "tcgen05, one CTA per chain (state in registers, products in tensor memory)",
+               "dv_tile": "mma.sync, one CTA per (chain, dv tile)", "-": "fused fp32 kernel"}
 
 
 def launches_per_call(w) -> int:
@@ -411,7 +425,8 @@ def bench_cuda(args, w, rank, world, local_rank):
     if w.prologue:  # raw q, k and gate inputs through the fused prologue
         def fwd(q, k, v, a, b, h0, o, hT, **kw):
             return lap.gdn_chunk_fwd_prologue(q, k, v, a, b, None, None, h0, o, hT, **kw)
-    extra = {"tc_chain": True} if args.tc_chain else {}
+    chain = chain_of(lap, w, args.chain)
+    extra = {} if w.dtype == "f32" or args.chain == "auto" else {"tc_chain": args.chain == "tc"}
 
     def step():
         fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
@@ -439,6 +454,8 @@ def bench_cuda(args, w, rank, world, local_rank):
         torch.distributed.barrier()
     ms = [a.elapsed_time(b) for a, b in evs]
     clk = clocks.stop()
+    # a bounded device-side wait that gave up, or an operand out of range, voids the run
+    lap.gdn_device_status(stream)
     local_ms = sum(ms)
     job_ms, job_tokens = reduce_timing(local_ms, float(w.T_total * args.steps))
     value = job_tokens / (job_ms / 1e3)
@@ -467,6 +484,7 @@ def bench_cuda(args, w, rank, world, local_rank):
     e2e_value = e2e_tok / (e2e_ms / 1e3)
 
     decode = run_decode(lap, WORKLOADS[args.decode_workload], dev) if args.decode else None
+    lap.gdn_device_status(stream)  # the end-to-end and decode runs as well
 
     if rank != 0:
         return
@@ -478,13 +496,12 @@ def bench_cuda(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, world, {"chain": "tcgen05 (state in tensor memory)"
-                                       if args.tc_chain else "mma.sync (dv tiles)"}),
+        "config": config_of(w, world, {"chain": CHAIN_LABEL[chain]}),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": measured_traffic(w.name + (":tc" if args.tc_chain else "")),
+                     "traffic": measured_traffic(w.name + (":tc" if chain == "tc" else "")),
                      "peak_source": src,
-                     "kernel": kernel_name(w, args.tc_chain),
+                     "kernel": kernel_name(w, chain),
                      "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],
                      "tensor_frac": round(model["flops"] / avg_s / 1e12 / peaks["bf16_tflops"], 4),
@@ -530,8 +547,9 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=0.5)
     ap.add_argument("--no-decode", dest="decode", action="store_false")
-    ap.add_argument("--tc-chain", action="store_true",
-                    help="run the chunk-serial operators on the tensor-memory chain")
+    ap.add_argument("--chain", default="auto", choices=["auto", "tc", "dv_tile"],
+                    help="chunk-serial kernel of the bf16 forward: the library's own choice "
+                         "(default), the tensor-memory chain, or the dv-tile chain")
     ap.add_argument("--decode-workload", default="long_64k_weak", choices=sorted(WORKLOADS),
                     help="state shape of the decode measurement (continues from its prefill)")
     args = ap.parse_args()

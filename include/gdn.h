@@ -65,15 +65,21 @@ enum {
    * going down; a violation is reported by the next gdn_device_status as
    * GDN_ERR_INVALID_ARG (the call itself still runs) */
   GDN_FLAG_CHECK_INPUTS = 2u,
-  /* the chunk-serial operators on the 5th-generation tensor cores with the
-   * fp32 state resident in tensor memory: one CTA per (sequence, v head), the
-   * one-chunk lookahead form of the state read (the forwards' _ex entry points;
-   * KDA returns GDN_ERR_UNSUPPORTED).  Same function and tolerances; uses one SM
-   * per chain where the dv-tile chain uses dv / 16 (or / 32), so it pays off when
-   * many chains share the GPU.  Without the flag every forward picks it by
-   * itself when the dv-tile chain would need several times more waves of CTAs
-   * over the SMs (e.g. 8 packed sequences x 32 v heads). */
-  GDN_FLAG_TC_CHAIN = 4u
+  /* the chunk-serial operators on the 5th-generation tensor cores: one CTA per
+   * (sequence, v head), the fp32 state in registers, every product's left
+   * factor and accumulator in tensor memory, the one-chunk lookahead form of
+   * the state read (the forwards' _ex entry points; KDA returns
+   * GDN_ERR_UNSUPPORTED).  Same function and tolerances; uses one SM per chain
+   * where the dv-tile chain uses dv / 16 (or / 32), so it pays off when many
+   * chains share the GPU.  Without either chain flag every forward picks one
+   * by itself from the number of chains (the tensor-memory chain once the
+   * dv-tile chain would need more waves of CTAs over the SMs than it saves
+   * per chunk). */
+  GDN_FLAG_TC_CHAIN = 4u,
+  /* the dv-tile chain (warp-level MMAs, dv / 16 or dv / 32 CTAs per chain)
+   * whatever the automatic choice; with GDN_FLAG_TC_CHAIN as well the call is
+   * GDN_ERR_INVALID_ARG */
+  GDN_FLAG_DV_TILE_CHAIN = 8u
 };
 
 typedef enum {
@@ -122,12 +128,22 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
  * be passed).  The bf16 forward runs in two launches: the chunk-parallel
  * operators #1-#4 (Gate, KKT, Solve, W/U) write one record per (64-token
  * chunk, v head) - W, diag(e) K, P, U^T and diag(scale gamma) Q in fp16 plus
- * the gate factors (72.6 KiB at d = 128; 80.6 KiB with GDN_FLAG_TC_CHAIN, whose
- * records add the lookahead tile X) - and the chunk-serial launch (#5 H with
- * #6 O) reads them.  Returns 0 for sizes gdn_chunk_fwd would reject.
+ * the gate factors (72.6 KiB at d = 128; 80.6 KiB for the tensor-memory chain,
+ * whose records add the lookahead tile X) - and the chunk-serial launch (#5 H
+ * with #6 O) reads them.  Returns 0 for sizes gdn_chunk_fwd would reject.
  */
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, int chunk,
                                     int has_cu_seqlens);
+
+/*
+ * gdn_chunk_fwd_chain_kind - which chunk-serial kernel a bf16 forward runs for
+ * n_seqs sequences (B, or the number of packed sequences) of Hv v heads with
+ * these head dims and flags: 1 the tensor-memory chain, 0 the dv-tile chain,
+ * -1 for sizes or flags the forward would reject.  delta_rule: 1 for
+ * gdn_chunk_fwd(_prologue)(_ex), 0 for ssd_chunk_fwd(_ex).  Host only; KDA
+ * forwards always run the dv-tile chain.
+ */
+int gdn_chunk_fwd_chain_kind(int n_seqs, int Hv, int dk, int dv, int delta_rule, unsigned flags);
 
 /*
  * gdn_chunk_fwd_ex - gdn_chunk_fwd with `flags` (GDN_FLAG_*: the GQA map, the

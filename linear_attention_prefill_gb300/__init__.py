@@ -6,13 +6,13 @@ workloads and the algorithmic byte/FLOP model.  The same kernels also run the
 Mamba-2 SSD scan (the recurrence without the delta rule's erase term), and Kimi
 Delta Attention (the delta rule with a per-key-channel gate) shares the chain.
 """
-from .binding import (GdnError, HostPipeline, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_prologue,
+from .binding import (GdnError, HostPipeline, chain_kind, gdn_chunk_fwd, gdn_chunk_fwd_host, gdn_chunk_fwd_prologue,
                       gdn_chunk_fwd_workspace_size, gdn_recurrent_step_prologue,
                       gdn_device_status, gdn_recurrent_step, gdn_selftest_expired_wait,
                       kda_chunk_fwd, kda_chunk_fwd_workspace_size, kda_recurrent_step,
                       load_library, ssd_chunk_fwd, ssd_recurrent_step, status_string)
 
-__all__ = ["GdnError", "HostPipeline", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_prologue",
+__all__ = ["GdnError", "HostPipeline", "chain_kind", "gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_prologue",
            "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step_prologue",
            "gdn_device_status", "gdn_recurrent_step", "gdn_selftest_expired_wait", "load_library",
            "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",

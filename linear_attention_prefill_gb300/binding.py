@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(5)
 # flags of gdn_chunk_fwd_ex / gdn_recurrent_step_ex (include/gdn.h)
 GDN_FLAG_HEAD_MAP_MODULO, GDN_FLAG_CHECK_INPUTS, GDN_FLAG_TC_CHAIN = 1, 2, 4
+GDN_FLAG_DV_TILE_CHAIN = 8
 
 # name -> (restype, argtypes) of every symbol include/gdn.h declares
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -54,6 +55,7 @@ SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [_I]),
     "gdn_last_error": (ctypes.c_char_p, []),
     "gdn_abi_version": (_I, []),
+    "gdn_chunk_fwd_chain_kind": (_I, [_I, _I, _I, _I, _I, _U]),
 }
 
 _lib = None
@@ -122,10 +124,23 @@ def gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, chunk=64, varlen=False) 
                                                            int(bool(varlen))))
 
 
+def chain_kind(n_seqs, Hv, dk, dv, op="gdn", tc_chain=None) -> str:
+    """The chunk-serial kernel a bf16 forward of ``op`` ("gdn", "gdn_prologue", "ssd" or
+    "kda") runs for n_seqs sequences of Hv v heads: "tc" (tensor-memory chain) or
+    "dv_tile"."""
+    if op == "kda":
+        return "dv_tile"
+    k = load_library().gdn_chunk_fwd_chain_kind(n_seqs, Hv, dk, dv, int(op != "ssd"),
+                                                _flags(tc_chain=tc_chain))
+    if k < 0:
+        raise ValueError(f"no chain for n_seqs={n_seqs}, Hv={Hv}, dk={dk}, dv={dv}")
+    return "tc" if k == 1 else "dv_tile"
+
+
 def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: Optional[float] = None, cu_seqlens=None, output_final_state=True,
                   stream=None, workspace=None, head_map: str = "grouped",
-                  check_inputs: bool = False, tc_chain: bool = False):
+                  check_inputs: bool = False, tc_chain: Optional[bool] = None):
     """Chunked-prefill forward of the gated delta rule; returns (o, hT).
 
     q, k [B, T, Hqk, dk]; v [B, T, Hv, dv] (bf16 or fp32, all the same);
@@ -136,9 +151,10 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
     least gdn_chunk_fwd_workspace_size bytes) or a fresh one from torch's
     caching allocator, and the flags: ``head_map`` "grouped" (hv // (Hv // Hqk))
     or "modulo" (hv % Hqk), ``check_inputs`` (a device pass over g, beta and
-    cu_seqlens, reported by gdn_device_status), ``tc_chain`` (the chunk-serial
-    operators on tcgen05 with the state in tensor memory).  ``scale`` defaults
-    to dk^-0.5.
+    cu_seqlens, reported by gdn_device_status), ``tc_chain`` (None: the library
+    picks the chain kind from the number of chains; True: the chunk-serial
+    operators on tcgen05, one CTA per chain; False: the dv-tile chain).
+    ``scale`` defaults to dk^-0.5.
     """
     flags = _flags(head_map, check_inputs, tc_chain)
     if flags and q.dtype != torch.bfloat16:
@@ -148,19 +164,23 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64
                       output_final_state, stream, workspace, flags=flags)
 
 
-def _flags(head_map="grouped", check_inputs=False, tc_chain=False) -> int:
+def _flags(head_map="grouped", check_inputs=False, tc_chain=None) -> int:
+    """The _ex flag word; ``tc_chain`` None lets the library pick the chain kind, True
+    forces the tensor-memory chain, False the dv-tile chain."""
     if head_map not in ("grouped", "modulo"):
         raise ValueError(f"head_map must be 'grouped' or 'modulo', got {head_map!r}")
+    if tc_chain not in (None, True, False):
+        raise ValueError(f"tc_chain must be None, True or False, got {tc_chain!r}")
     return ((GDN_FLAG_HEAD_MAP_MODULO if head_map == "modulo" else 0)
             | (GDN_FLAG_CHECK_INPUTS if check_inputs else 0)
-            | (GDN_FLAG_TC_CHAIN if tc_chain else 0))
+            | (0 if tc_chain is None else GDN_FLAG_TC_CHAIN if tc_chain else GDN_FLAG_DV_TILE_CHAIN))
 
 
 def gdn_chunk_fwd_prologue(q, k, v, a, b, A_log=None, dt_bias=None, h0=None, o=None, hT=None, *,
                            chunk: int = 64, scale: Optional[float] = None, cu_seqlens=None,
                            output_final_state=True, stream=None, workspace=None,
                            head_map: str = "grouped", check_inputs: bool = False,
-                           tc_chain: bool = False):
+                           tc_chain: Optional[bool] = None):
     """gdn_chunk_fwd with the fused prologue (bf16): q, k unnormalised; raw gates a, b
     [B, T, Hv] fp32; A_log, dt_bias [Hv] fp32 or None.  g = -exp(A_log) softplus(a +
     dt_bias), beta = sigmoid(b), q and k divided by sqrt(sum x^2 + 1e-6).  Returns (o, hT)."""
@@ -178,7 +198,7 @@ def gdn_chunk_fwd_prologue(q, k, v, a, b, A_log=None, dt_bias=None, h0=None, o=N
 def ssd_chunk_fwd(q, k, v, g, beta, h0=None, o=None, hT=None, *, chunk: int = 64,
                   scale: float = 1.0, cu_seqlens=None, output_final_state=True, stream=None,
                   workspace=None, head_map: str = "grouped", check_inputs: bool = False,
-                  tc_chain: bool = False):
+                  tc_chain: Optional[bool] = None):
     """Chunked Mamba-2 SSD scan (the same recurrence without the erase term):
     S_t = exp(g_t) S_{t-1} + beta_t v_t k_t^T, o_t = S_t (scale q_t), with
     C -> q, B -> k, x -> v, dt A -> g, dt -> beta.  Arguments as gdn_chunk_fwd;

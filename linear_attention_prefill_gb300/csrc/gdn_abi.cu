@@ -150,16 +150,19 @@ gdn_status check_fwd(const void* q, const void* k, const void* v, const float* g
   return GDN_OK;
 }
 
-constexpr unsigned kFwdFlags = GDN_FLAG_HEAD_MAP_MODULO | GDN_FLAG_CHECK_INPUTS | GDN_FLAG_TC_CHAIN;
+constexpr unsigned kFwdFlags =
+    GDN_FLAG_HEAD_MAP_MODULO | GDN_FLAG_CHECK_INPUTS | GDN_FLAG_TC_CHAIN | GDN_FLAG_DV_TILE_CHAIN;
 
 // Applies the flags of an _ex forward to p; `tc_ok` says whether the tcgen05 chain
 // exists for this operation.
 gdn_status apply_flags(unsigned flags, bool tc_ok, gdn::FwdParams* p) {
   if (flags & ~kFwdFlags) return fail(GDN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kFwdFlags);
+  if ((flags & GDN_FLAG_TC_CHAIN) && (flags & GDN_FLAG_DV_TILE_CHAIN))
+    return fail(GDN_ERR_INVALID_ARG, "GDN_FLAG_TC_CHAIN and GDN_FLAG_DV_TILE_CHAIN together");
   if ((flags & GDN_FLAG_TC_CHAIN) && !tc_ok)
     return fail(GDN_ERR_UNSUPPORTED, "GDN_FLAG_TC_CHAIN: no tensor-memory chain for this operation");
   p->head_map = (flags & GDN_FLAG_HEAD_MAP_MODULO) ? 1 : 0;
-  p->tc_chain = (flags & GDN_FLAG_TC_CHAIN) ? 1 : 0;
+  p->tc_chain = (flags & GDN_FLAG_TC_CHAIN) ? 1 : (flags & GDN_FLAG_DV_TILE_CHAIN) ? -1 : 0;
   return GDN_OK;
 }
 
@@ -237,7 +240,8 @@ gdn_status run_fwd_bf16(const gdn::FwdParams& p, void* ws, size_t ws_size, cudaS
     return fail(GDN_ERR_UNSUPPORTED, "%lld tokens: the bf16 path takes at most 2^31 - 1",
                 (p.cu_seqlens ? 1ll : (long long)p.N) * p.T);
   gdn::FwdParams q = p;
-  if (!q.tc_chain && gdn::tc_chain_pays(q)) q.tc_chain = 1;  // many chains: one CTA each
+  // the chain kind: forced by a flag (1 / -1), else by the number of chains
+  q.tc_chain = q.tc_chain > 0 || (q.tc_chain == 0 && gdn::tc_chain_pays(q)) ? 1 : 0;
   const gdn::WsLayout w = gdn::ws_layout(q, ws);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % 256) != 0 || ws_size < gdn::ws_bytes(w, p.Hv))
     return fail(GDN_ERR_INVALID_ARG, "workspace %p of %zu bytes: need %zu bytes, 256-byte aligned",
@@ -336,6 +340,22 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int d
                 has_cu_seqlens ? &fake_cu : nullptr, 2, &p) != GDN_OK)
     return 0;
   return gdn::ws_bytes_any(p);
+}
+
+int gdn_chunk_fwd_chain_kind(int n_seqs, int Hv, int dk, int dv, int delta_rule, unsigned flags) {
+  if (n_seqs < 0 || Hv <= 0 || (dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return -1;
+  if ((flags & ~kFwdFlags) ||
+      ((flags & GDN_FLAG_TC_CHAIN) && (flags & GDN_FLAG_DV_TILE_CHAIN)))
+    return -1;
+  if (flags & GDN_FLAG_TC_CHAIN) return 1;
+  if (flags & GDN_FLAG_DV_TILE_CHAIN) return 0;
+  gdn::FwdParams p{};
+  p.N = n_seqs;
+  p.Hv = Hv;
+  p.dk = dk;
+  p.dv = dv;
+  p.delta_rule = delta_rule ? 1 : 0;
+  return gdn::tc_chain_pays(p) ? 1 : 0;
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,

@@ -37,8 +37,10 @@ struct FwdParams {
   int kda;
   // GQA map: 0 grouped (v head hv reads q/k head hv / (Hv / Hqk)), 1 modulo (hv % Hqk)
   int head_map;
-  // 1: the tcgen05 chain (one CTA per chain, the state in tensor memory, lookahead
-  // records); 0: the mma.sync chain (dv tiles, one CTA each)
+  // the chain kind: 1 the tcgen05 chain (one CTA per chain, the fp32 state in the
+  // registers of its state warps, products in tensor memory, lookahead records); 0 the
+  // mma.sync chain (dv tiles, one CTA each); as a flag of a call, -1 forces the
+  // mma.sync chain and 0 leaves the choice to tc_chain_pays
   int tc_chain;
 };
 constexpr float kNormEps = 1e-6f;
@@ -160,17 +162,17 @@ inline int dv_tile(const FwdParams& p) {
   return 32;
 }
 
-// Which chain runs when the caller does not ask for the tcgen05 one: the mma.sync
-// chain walks one CTA per (chain, dv tile) at ~0.95 us a chunk, the tcgen05 chain one
-// CTA per chain at ~2.2 us a chunk (measured on GB300), so the tcgen05 chain is taken
-// when the mma.sync chain would need that many more waves of CTAs over the SMs.  KDA
-// records exist for the mma.sync chain only.
+// Which chain runs when the caller forces neither: the mma.sync chain walks one CTA
+// per (chain, dv tile) at ~0.93 us a chunk, the tcgen05 chain one CTA per chain at
+// ~1.72 us a chunk (both measured on GB300 at d = 128), so the tcgen05 chain is taken
+// when the mma.sync chain would need about twice as many waves of CTAs over the SMs.
+// KDA records exist for the mma.sync chain only.
 inline bool tc_chain_pays(const FwdParams& p) {
   if (p.kda) return false;
   const long long chains = (long long)p.N * p.Hv;
   const long long tiles = p.dv / dv_tile(p);
   const long long waves_mma = (chains * tiles + 151) / 152, waves_tc = (chains + 151) / 152;
-  return 22 * waves_tc < 95 * waves_mma / 10;
+  return 172 * waves_tc < 93 * waves_mma;
 }
 
 // Layout for one call (sizes validated); base may be null when only sizing.

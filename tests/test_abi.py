@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
                  "ssd_chunk_fwd_f32", "ssd_recurrent_step", "ssd_recurrent_step_f32",
                  "gdn_chunk_fwd_prologue", "gdn_chunk_fwd_prologue_ex",
                  "gdn_recurrent_step_prologue", "gdn_selftest_expired_wait", "kda_chunk_fwd",
-                 "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size", "kda_recurrent_step"):
+                 "kda_chunk_fwd_ex", "kda_chunk_fwd_workspace_size", "kda_recurrent_step",
+                 "gdn_chunk_fwd_chain_kind"):
         assert want in names
 
 
@@ -156,7 +157,7 @@ def test_ex_rejects_small_or_misaligned_workspace(lib):
     need = lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
     args = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
     # the size function covers every flag; a call checks what its own records need
-    for flags in (0, 1, 2, 4, 7):
+    for flags in (0, 1, 2, 4, 7, 8, 11):
         assert lib.gdn_chunk_fwd_ex(*args, flags, None, need, None) == 1
         assert lib.gdn_chunk_fwd_ex(*args, flags, A, need // 2, None) == 1
         assert lib.gdn_chunk_fwd_ex(*args, flags, A + 16, need, None) == 1
@@ -167,8 +168,11 @@ def test_ex_rejects_small_or_misaligned_workspace(lib):
 def test_ex_rejects_unknown_flags(lib):
     need = lib.gdn_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
     args = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
-    assert lib.gdn_chunk_fwd_ex(*args, 8, A, need, None) == 1
+    assert lib.gdn_chunk_fwd_ex(*args, 16, A, need, None) == 1
     assert b"flag" in lib.gdn_last_error()
+    # the two chain flags exclude each other
+    assert lib.gdn_chunk_fwd_ex(*args, 12, A, need, None) == 1
+    assert b"together" in lib.gdn_last_error()
     # the decode step takes the head map and the input check, not the chain choice
     sargs = (A, A, A, A, A, A, A, 1, 1, 2, 128, 128, 0.088)
     assert lib.gdn_recurrent_step_ex(*sargs, 4, None) == 1
@@ -179,7 +183,25 @@ def test_ex_rejects_unknown_flags(lib):
     kargs = (A, A, A, A, A, None, A, None, 1, 128, 1, 2, 128, 128, 64, 0.088, None)
     kneed = lib.kda_chunk_fwd_workspace_size(1, 128, 1, 2, 128, 128, 64, 0)
     assert lib.kda_chunk_fwd_ex(*kargs, 4, A, kneed, None) == 2
-    assert lib.ssd_chunk_fwd_ex(*kargs, 8, A, need, None) == 1
+    assert lib.ssd_chunk_fwd_ex(*kargs, 16, A, need, None) == 1
+
+
+def test_chain_kind(lib):
+    """The chain choice: forced by a flag, else the dv-tile chain while its CTAs fit in few
+    waves over the 152 SMs and the tensor-memory chain once they do not; never for KDA."""
+    kind = lib.gdn_chunk_fwd_chain_kind
+    assert kind(1, 16, 128, 128, 1, 0) == 0      # 16 chains
+    assert kind(1, 32, 128, 128, 1, 0) == 0      # 32 chains
+    assert kind(8, 32, 128, 128, 1, 0) == 1      # 256 chains
+    assert kind(1, 16, 128, 128, 1, 4) == 1      # forced
+    assert kind(8, 32, 128, 128, 1, 8) == 0      # forced
+    assert kind(1, 16, 128, 128, 1, 12) == -1    # both
+    assert kind(1, 16, 128, 128, 1, 16) == -1    # unknown bit
+    assert kind(1, 16, 96, 128, 1, 0) == -1      # unsupported head dim
+    import linear_attention_prefill_gb300 as lap
+    assert lap.chain_kind(8, 32, 128, 128, "kda") == "dv_tile"
+    assert lap.chain_kind(8, 32, 128, 128) == "tc"
+    assert lap.chain_kind(8, 32, 128, 128, tc_chain=False) == "dv_tile"
 
 
 @pytest.mark.parametrize("case,status", [

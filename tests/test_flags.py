@@ -67,14 +67,24 @@ def test_tc_chain_strong_and_weak_decay(cuda_lib, g_mu, g_scale):
     check_heads(x, o, hT, heads=range(2), dtype="bf16")
 
 
-def test_tc_chain_matches_the_default_chain(cuda_lib):
+def test_tc_chain_matches_the_dv_tile_chain(cuda_lib):
     """Both chains compute the same function: within the tolerance of each other."""
     w = Workload("tc", (500,), 2, 4, 128, 128, 64, "bf16", h0_std=0.1, seed=114)
     x = make_inputs(w, device="cuda")
-    o1, h1 = run(cuda_lib, x)
+    o1, h1 = run(cuda_lib, x, tc_chain=False)
     o2, h2 = run(cuda_lib, x, tc_chain=True)
     assert record("tc_vs_default", "o", to_np(o2), to_np(o1)) < TOL["bf16"]
     assert record("tc_vs_default", "hT", to_np(h2), to_np(h1)) < TOL["bf16"]
+
+
+def test_dv_tile_chain_forced_on_many_chains(cuda_lib):
+    """256 packed chains pick the tensor-memory chain by themselves; forcing the dv-tile
+    chain there gives the same function."""
+    w = WORKLOADS["varlen_8seq"]
+    assert cuda_lib.chain_kind(w.n_seqs, w.Hv, w.dk, w.dv) == "tc"
+    x = make_inputs(w, device="cuda")
+    o, hT = run(cuda_lib, x, tc_chain=False)
+    check_heads(x, o, hT, [0, 31], "bf16", seqs=[0, 3, 7])
 
 
 @pytest.mark.parametrize("name,heads", [("layer_16h_4k", [0, 9, 15]),
