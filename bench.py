@@ -50,17 +50,18 @@ from linear_attention_prefill_gb300.workloads import HEADLINE, WORKLOADS, make_d
 METRIC = "GDN chunked-prefill tokens/s per layer on 1 GB300; % of TC/HBM roofline"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 320 * 2 ** 20
-# One bf16 forward call is two launches on the caller's stream (the chunk-parallel
-# prep kernel, then the chunk-serial chain kernel that also writes o); the fp32 path
-# is one fused launch.  The roofline block times the call, and the launch list in
-# profiles/ gives each kernel's share.
+# One forward call is two launches on the caller's stream (the chunk-parallel prep
+# kernel, then the chunk-serial chain kernel that also writes o), in bf16 and fp32
+# alike.  The roofline block times the call, and the launch list in profiles/ gives
+# each kernel's share.
 KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
 KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
                 "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
                 "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
                                 "gdn_chain_kernel)",
-                "f32": "gdn_chunk_fwd_f32 (gdn_fwd_f32_kernel)",
-                "ssd_f32": "ssd_chunk_fwd_f32 (gdn_fwd_f32_kernel, no erase term)"}
+                "f32": "gdn_chunk_fwd_f32 (gdn_prep_f32_kernel + gdn_chain_f32_kernel)",
+                "ssd_f32": "ssd_chunk_fwd_f32 (gdn_prep_f32_kernel + gdn_chain_f32_kernel, no erase "
+                           "term)"}
 
 
 def kernel_name(w, chain="dv_tile") -> str:
@@ -82,13 +83,14 @@ def chain_of(lap, w, choice) -> str:
 
 
 CHAIN_LABEL = {"tc": "tcgen05, one CTA per chain (state in registers, products in tensor memory)",
-               "dv_tile": "mma.sync, one CTA per (chain, dv tile)", "-": "fused fp32 kernel"}
+               "dv_tile": "mma.sync, one CTA per (chain, dv tile)",
+               "-": "fp32 FMA, one CTA per (chain, 16 dv columns)"}
 
 
 def launches_per_call(w) -> int:
-    """Kernel launches of one forward call: the fp32 path is one fused launch; the bf16
-    path a prep launch and a chain launch."""
-    return 1 if w.dtype == "f32" else 2
+    """Kernel launches of one forward call: a prep launch and a chain launch (bf16 and
+    fp32 paths alike)."""
+    return 2
 
 
 def measured_traffic(workload: str):

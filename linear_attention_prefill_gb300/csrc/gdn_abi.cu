@@ -219,11 +219,21 @@ gdn_status check_kda(const void* q, const void* k, const void* v, const float* g
   return GDN_OK;
 }
 
+// fp32 forward: the chunk-parallel prep and the chain, on fp32 records in a workspace
+// taken from the stream-ordered pool and given back after.
 gdn_status run_fwd_f32(const gdn::FwdParams& p, cudaStream_t stream) {
   if (p.N == 0) return GDN_OK;
   if (!p.cu_seqlens && p.T == 0) return empty_forward(p, stream);
-  cudaError_t e = gdn::launch_fwd_f32(p, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernel");
+  gdn::WsLayout w = gdn::ws_layout(p, nullptr);
+  const size_t bytes = (size_t)w.n_slots * p.Hv * gdn::f32_rec_bytes(p);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "allocating the workspace");
+  w = gdn::ws_layout(p, ws);
+  e = gdn::launch_fwd_f32(p, w, stream);
+  const cudaError_t ef = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the forward kernels");
+  if (ef != cudaSuccess) return cuda_fail(ef, "freeing the workspace");
   return GDN_OK;
 }
 

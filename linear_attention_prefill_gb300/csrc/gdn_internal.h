@@ -267,7 +267,10 @@ cudaError_t launch_chain_tc(const FwdParams& p, const WsLayout& ws, cudaStream_t
 // Input check of an _ex call (g, beta in their domains, cu_seqlens ordered): records
 // kErrInput in the device error word.
 cudaError_t launch_check_inputs(const FwdParams& p, cudaStream_t stream);
-cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+// The fp32 forward (gdn_fwd_f32.cu): fp32 records of f32_rec_bytes(p) per (chunk slot,
+// v head) in the slots of ws_layout(p, base), then the chain.
+size_t f32_rec_bytes(const FwdParams& p);
+cudaError_t launch_fwd_f32(const FwdParams& p, const WsLayout& ws, cudaStream_t stream);
 cudaError_t launch_step_bf16(const StepParams& p, cudaStream_t stream);
 cudaError_t launch_step_f32(const StepParams& p, cudaStream_t stream);
 

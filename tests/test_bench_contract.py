@@ -42,7 +42,7 @@ def test_reference_arm_line():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("workload,launches", [("layer_16h_4k", 2), ("tiny_f32", 1)])
+@pytest.mark.parametrize("workload,launches", [("layer_16h_4k", 2), ("tiny_f32", 2)])
 def test_cuda_arm_line(workload, launches):
     d = run_bench("--workload", workload, "--steps", "5", "--warmup", "3",
                   "--cpu-baseline-s", "0.3", "--no-decode")

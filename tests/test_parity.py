@@ -117,7 +117,7 @@ def test_split_resume_matches_one_call(cuda_lib, dtype):
          for k_, v_ in x.items()}
     b["h0"] = ha
     ob, hb = run(cuda_lib, b)
-    if dtype == "f32":  # one fused launch: both sides take the same roundings
+    if dtype == "f32":  # the fp32 state passes from chunk to chunk as from call to call
         assert torch.equal(torch.cat([oa, ob], dim=1), o)
         assert torch.equal(hb, hT)
     else:
