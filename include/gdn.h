@@ -170,9 +170,9 @@ gdn_status gdn_chunk_fwd_ex(const void* q, const void* k, const void* v, const f
  * synchronisation an allocation can imply, or code embedded in a runtime that
  * owns all device memory through its own pool.
  *  - Limit: gdn_chunk_fwd_workspace_size(...) must be at most 32 MiB (about
- *    450 chunk-and-v-head records of 72.6 KiB at dk = dv = 128, e.g. 4096
- *    tokens x 7 v heads); larger sizes return GDN_ERR_INVALID_ARG and launch
- *    nothing.
+ *    406 chunk-and-v-head records at dk = dv = 128: the size covers the
+ *    larger, 80.6 KiB record of the tensor-memory chain; e.g. 4096 tokens x 6
+ *    v heads); larger sizes return GDN_ERR_INVALID_ARG and launch nothing.
  *  - Every GPU that runs the library's device code keeps those 32 MiB until
  *    the process exits.
  *  - Every call looks up the array's device address on the current device
