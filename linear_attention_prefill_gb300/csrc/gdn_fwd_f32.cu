@@ -1,8 +1,7 @@
 // gdn_fwd_f32.cu - chunked-prefill forward with fp32 q/k/v/o (fp32 throughout).
 //
 // The operators of "Empowering Hybrid Attention Models on NPUs", §2.1 / Figure
-// 1(b), in two launches like the bf16 path, every product an fp32 FMA on the
-// CUDA cores:
+// 1(b), in two launches like the bf16 path:
 //
 //  * gdn_prep_f32_kernel - one CTA per (64-token chunk, v head), all chunks in
 //    parallel: #1 Gate (cumsum of g, gamma, e), #2 KKT and the QK^T gram P, #3
@@ -11,9 +10,18 @@
 //    task in the workspace.
 //  * gdn_chain_f32_kernel - one CTA per (sequence, v head, 16 dv columns), the
 //    chunks in order with the state tile h[:, tile] on chip and the next chunk's
-//    record loading meanwhile: #5 V_new = U - W h,
-//    #6 O = Q~ h + P V_new, then the in-place update h = gamma_last h + Kt^T V_new
-//    (the chunk-first order of §5, Figure 10(b)).
+//    record loading meanwhile: #5 V_new = U - W h, #6 O = Q~ h + P V_new, then
+//    the in-place update h = gamma_last h + Kt^T V_new (the chunk-first order of
+//    §5, Figure 10(b)).
+//
+// Every matrix product runs on the tensor cores in three tf32 MMAs (m16n8k8)
+// per step: each fp32 operand is split into a tf32 part and a tf32 remainder,
+// x = hi + lo, and A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi with fp32
+// accumulation (the split-precision method of Ootomo and Yokota, "Recovering
+// single precision accuracy from Tensor Cores while surpassing the FP32
+// theoretical peak performance", 2022): about 21 significant bits per product,
+// well inside the fp32 path's tolerance.  The triangular solve and the gates stay
+// fp32 on the CUDA cores.
 //
 // Without the delta rule's erase term (the Mamba-2 scan) A = 0, so Tm = I and the
 // chain takes V_new = U = diag(beta) V.
@@ -26,6 +34,59 @@ namespace {
 constexpr int kC = 64;
 constexpr int kThreads = 256;
 constexpr int kTile = 16;  // dv columns per chain CTA
+
+// ---- split-precision tf32 MMA ------------------------------------------------
+__device__ __forceinline__ uint32_t f2tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo: hi = tf32(x), lo = tf32(x - hi)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = f2tf32(x);
+  lo = f2tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// d += A B for one m16n8k8 step from fp32 fragments (the register layout of the tf32
+// MMA: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
+// d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]; g = lane / 4, t = lane % 4)
+__device__ __forceinline__ void mma3(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
+  mma_tf32(d, al, bh);  // the small terms first
+  mma_tf32(d, ah, bl);
+  mma_tf32(d, ah, bh);
+}
+// A fragment of rows r0.., columns k0.. of a row-major matrix with row stride ld
+__device__ __forceinline__ void frag_a(float (&a)[4], const float* A, int ld, int r0, int k0,
+                                       int g, int t) {
+  a[0] = A[(r0 + g) * ld + k0 + t];
+  a[1] = A[(r0 + g + 8) * ld + k0 + t];
+  a[2] = A[(r0 + g) * ld + k0 + t + 4];
+  a[3] = A[(r0 + g + 8) * ld + k0 + t + 4];
+}
+// B fragment of B[k][n] stored row-major [k][n] (stride ld), rows k0.., columns n0..
+__device__ __forceinline__ void frag_b_kn(float (&b)[2], const float* B, int ld, int k0, int n0,
+                                          int g, int t) {
+  b[0] = B[(k0 + t) * ld + n0 + g];
+  b[1] = B[(k0 + t + 4) * ld + n0 + g];
+}
+// B fragment of B[k][n] = M[n][k] for M stored row-major [n][k] (stride ld)
+__device__ __forceinline__ void frag_b_nk(float (&b)[2], const float* M, int ld, int k0, int n0,
+                                          int g, int t) {
+  b[0] = M[(n0 + g) * ld + k0 + t];
+  b[1] = M[(n0 + g) * ld + k0 + t + 4];
+}
 
 // fp32 record of one (chunk slot, v head), offsets in floats; every piece is a
 // multiple of 4 floats (16 bytes) long.
@@ -44,13 +105,14 @@ struct RecF32 {
 // prep: one chunk of one v head
 template <int DK, int DV>
 struct PrepSmem {
-  static constexpr int LDK = DK + 1, LDV = DV + 1, LDA = kC + 1;  // odd strides
+  // row strides: 4 mod 32 for the A-operand rows (fragment rows g, columns t), 8 mod 32
+  // for V, read as a [k][n] B operand (rows t, columns g)
+  static constexpr int LDK = DK + 4, LDV = DV + 8, LDA = kC + 4;
   float K[kC * LDK];
   float Q[kC * LDK];
   float V[kC * LDV];
   float A[kC * LDA];  // strictly lower A
   float Tm[kC * LDA];
-  float P[kC * LDA];
   float X[3 * 256];   // solve scratch
   float g[kC], beta[kC], G[kC], gam[kC], e[kC];
 };
@@ -63,7 +125,7 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
   extern __shared__ __align__(16) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ti = tid >> 4, tj = tid & 15;  // 16 x 16 thread grid for register tiles
+  const int fg = lane >> 2, ft = lane & 3;  // MMA fragment row / column group
 
   const int hv = blockIdx.x % p.Hv;
   const long long slot = blockIdx.x / p.Hv;
@@ -109,16 +171,13 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
 #pragma unroll
     for (int i = 0; i < NK; ++i) {
       const int e4 = tid + i * kThreads, rr = (4 * e4) / DK, d = (4 * e4) % DK;
-      float* kd = &s.K[rr * LDK + d];
-      float* qd = &s.Q[rr * LDK + d];
-      kd[0] = kr[i].x, kd[1] = kr[i].y, kd[2] = kr[i].z, kd[3] = kr[i].w;
-      qd[0] = qr[i].x, qd[1] = qr[i].y, qd[2] = qr[i].z, qd[3] = qr[i].w;
+      *reinterpret_cast<float4*>(&s.K[rr * LDK + d]) = kr[i];
+      *reinterpret_cast<float4*>(&s.Q[rr * LDK + d]) = qr[i];
     }
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e4 = tid + i * kThreads, rr = (4 * e4) / DV, d = (4 * e4) % DV;
-      float* vd = &s.V[rr * LDV + d];
-      vd[0] = vr[i].x, vd[1] = vr[i].y, vd[2] = vr[i].z, vd[3] = vr[i].w;
+      *reinterpret_cast<float4*>(&s.V[rr * LDV + d]) = vr[i];
     }
     if (tid < kC) {
       s.g[tid] = gv;
@@ -148,39 +207,38 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
   }
   __syncthreads();
 
-  // ---- #2 KK^T and QK^T: thread (ti, tj) owns rows ti + 16a, columns tj + 16b
+  // ---- #2 KK^T and QK^T: warp w takes rows 16 (w % 4) of K (w < 4) or of Q (w >= 4)
+  // against all 64 keys: 8 n-tiles of 8 columns, DK / 8 k-steps
   {
-    float sk[4][4] = {}, sq[4][4] = {};
-    for (int d = 0; d < DK; ++d) {
-      float kr[4], qr[4], kc[4];
+    const bool isQ = warp >= 4;
+    const int r0 = 16 * (warp & 3);
+    const float* Arows = isQ ? s.Q : s.K;
+    float acc[8][4] = {};
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        kr[a] = s.K[(ti + 16 * a) * LDK + d];
-        qr[a] = s.Q[(ti + 16 * a) * LDK + d];
-        kc[a] = s.K[(tj + 16 * a) * LDK + d];
+    for (int k0 = 0; k0 < DK; k0 += 8) {
+      float a[4];
+      frag_a(a, Arows, LDK, r0, k0, fg, ft);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        float b[2];
+        frag_b_nk(b, s.K, LDK, k0, 8 * nt, fg, ft);
+        mma3(acc[nt], a, b);
       }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          sk[a][b] += kr[a] * kc[b];
-          sq[a][b] += qr[a] * kc[b];
-        }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int r = ti + 16 * a, cc = tj + 16 * b;
+      for (int i = 0; i < 4; ++i) {
+        const int r = r0 + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
         const bool low = r >= cc && r < L;
         const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
-        s.A[r * LDA + cc] = (low && r > cc && delta) ? s.beta[r] * m * sk[a][b] : 0.f;
-        const float pv = low ? p.scale * m * sq[a][b] : 0.f;
-        s.P[r * LDA + cc] = pv;
-        rec[R::P + r * kC + cc] = pv;
+        if (isQ)
+          rec[R::P + r * kC + cc] = low ? p.scale * m * acc[nt][i] : 0.f;
+        else
+          s.A[r * LDA + cc] = (low && r > cc && delta) ? s.beta[r] * m * acc[nt][i] : 0.f;
       }
   }
-  // Kt^T and Q~ go out while the grams are formed
+  // Kt^T and Q~ go out while the others finish the grams
   for (int i = tid; i < kC * DK; i += kThreads) {
     const int r = i / DK, d = i % DK;  // token r, channel d
     rec[R::Qt + r * DK + d] = p.scale * s.gam[r] * s.Q[r * LDK + d];
@@ -189,49 +247,66 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
   }
   __syncthreads();
 
-  // ---- #3 Solve: Tm = (I + A)^-1
+  // ---- #3 Solve: Tm = (I + A)^-1 (fp32, CUDA cores)
   solve_unit_lower_64_f32<kThreads>(s.A, LDA, s.Tm, LDA, s.X);
 
-  // ---- #4 W = Tm diag(beta gamma) K, U = Tm diag(beta) V: rows ti + 16a, columns tj + 16b
-  if (delta) {
-    constexpr int NB = DK / 16;
-    float w[4][NB] = {};
-    for (int j = 0; j < kC; ++j) {
-      const float f = s.beta[j] * s.gam[j];
-      float tr[4], kc[NB];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) tr[a] = s.Tm[(ti + 16 * a) * LDA + j];
-#pragma unroll
-      for (int b = 0; b < NB; ++b) kc[b] = f * s.K[j * LDK + tj + 16 * b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < NB; ++b) w[a][b] += tr[a] * kc[b];
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < NB; ++b) rec[R::W + (ti + 16 * a) * DK + tj + 16 * b] = w[a][b];
-  }
+  // ---- #4 W = Tm diag(beta gamma) K, U = Tm diag(beta) V: warp w takes rows 16 (w % 4)
+  // and half w / 4 of the columns
   {
-    constexpr int NB = DV / 16;
-    float u[4][NB] = {};
-    for (int j = 0; j < kC; ++j) {
-      const float f = s.beta[j];
-      float tr[4], vc[NB];
+    const int r0 = 16 * (warp & 3), half = warp >> 2;
+    if (delta) {
+      constexpr int NT = DK / 16;  // n-tiles in a half
+      float acc[NT][4] = {};
 #pragma unroll
-      for (int a = 0; a < 4; ++a) tr[a] = s.Tm[(ti + 16 * a) * LDA + j];
+      for (int k0 = 0; k0 < kC; k0 += 8) {
+        float a[4];
+        frag_a(a, s.Tm, LDA, r0, k0, fg, ft);
+        const float f0 = s.beta[k0 + ft] * s.gam[k0 + ft];
+        const float f1 = s.beta[k0 + ft + 4] * s.gam[k0 + ft + 4];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) vc[b] = f * s.V[j * LDV + tj + 16 * b];
+        for (int nt = 0; nt < NT; ++nt) {
+          float b[2];
+          frag_b_kn(b, s.K, LDK, k0, half * (DK / 2) + 8 * nt, fg, ft);
+          b[0] *= f0;
+          b[1] *= f1;
+          mma3(acc[nt], a, b);
+        }
+      }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int b = 0; b < NB; ++b) u[a][b] += tr[a] * vc[b];
+        for (int h = 0; h < 2; ++h) {
+          const int r = r0 + fg + 8 * h, cc = half * (DK / 2) + 8 * nt + 2 * ft;
+          *reinterpret_cast<float2*>(&rec[R::W + r * DK + cc]) =
+              make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        }
     }
+    {
+      constexpr int NT = DV / 16;
+      float acc[NT][4] = {};
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+      for (int k0 = 0; k0 < kC; k0 += 8) {
+        float a[4];
+        frag_a(a, s.Tm, LDA, r0, k0, fg, ft);
+        const float f0 = s.beta[k0 + ft], f1 = s.beta[k0 + ft + 4];
 #pragma unroll
-      for (int b = 0; b < NB; ++b) rec[R::U + (ti + 16 * a) * DV + tj + 16 * b] = u[a][b];
+        for (int nt = 0; nt < NT; ++nt) {
+          float b[2];
+          frag_b_kn(b, s.V, LDV, k0, half * (DV / 2) + 8 * nt, fg, ft);
+          b[0] *= f0;
+          b[1] *= f1;
+          mma3(acc[nt], a, b);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = r0 + fg + 8 * h, cc = half * (DV / 2) + 8 * nt + 2 * ft;
+          *reinterpret_cast<float2*>(&rec[R::U + r * DV + cc]) =
+              make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+        }
+    }
   }
 }
 
@@ -239,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
 // chain: one (sequence, v head, 16-column dv tile), chunks in order
 template <int DK>
 struct ChainRec {  // one chunk's record pieces in shared memory
-  static constexpr int LDK = DK + 4, LDC = kC + 4;  // float4 rows, banks spread
+  static constexpr int LDK = DK + 4, LDC = kC + 4;  // A-operand rows: stride 4 mod 32
   float W[kC * LDK];
   float Qt[kC * LDK];
   float KtT[DK * LDC];
@@ -251,37 +326,11 @@ struct ChainRec {  // one chunk's record pieces in shared memory
 template <int DK>
 struct ChainSmem {
   static constexpr int kBufs = DK == 64 ? 2 : 1;
+  static constexpr int LDT = kTile + 8;  // B-operand rows [k][n]: stride 8 mod 32 (24)
   ChainRec<DK> rec[kBufs];
-  float H[DK * kTile];   // h[:, tile]
-  float Vn[kC * kTile];  // V_new[:, tile]
+  float H[DK * LDT];   // h[:, tile]
+  float Vn[kC * LDT];  // V_new[:, tile]
 };
-
-__device__ __forceinline__ float4 lds4(const float* a) { return *reinterpret_cast<const float4*>(a); }
-__device__ __forceinline__ void fma4(float4& acc, float a, const float4& b) {
-  acc.x = fmaf(a, b.x, acc.x);
-  acc.y = fmaf(a, b.y, acc.y);
-  acc.z = fmaf(a, b.z, acc.z);
-  acc.w = fmaf(a, b.w, acc.w);
-}
-// A[row][0..K) x B[0..K)[cg..cg+4), A row-major, B [K][kTile]; two accumulators (even
-// and odd groups of four k) halve the dependent FMA chain
-template <int K>
-__device__ __forceinline__ float4 row_times_tile(const float* arow, const float* B, int cg) {
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll 2
-  for (int k = 0; k < K; k += 8) {
-    const float4 x = lds4(arow + k), y = lds4(arow + k + 4);
-    fma4(a0, x.x, lds4(B + (k + 0) * kTile + cg));
-    fma4(a1, y.x, lds4(B + (k + 4) * kTile + cg));
-    fma4(a0, x.y, lds4(B + (k + 1) * kTile + cg));
-    fma4(a1, y.y, lds4(B + (k + 5) * kTile + cg));
-    fma4(a0, x.z, lds4(B + (k + 2) * kTile + cg));
-    fma4(a1, y.z, lds4(B + (k + 6) * kTile + cg));
-    fma4(a0, x.w, lds4(B + (k + 3) * kTile + cg));
-    fma4(a1, y.w, lds4(B + (k + 7) * kTile + cg));
-  }
-  return make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
-}
 
 // issue the cp.async copies of one chunk's record pieces (the caller commits)
 template <int DK, int DV, bool DELTA>
@@ -313,12 +362,14 @@ template <int DK, int DV, bool DELTA>
 __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams p, const WsLayout ws) {
   using S = ChainSmem<DK>;
   using R = RecF32<DK, DV>;
-  constexpr int LDK = ChainRec<DK>::LDK, LDC = ChainRec<DK>::LDC;
-  constexpr int RA = DK / 64;  // state rows of a thread in the update
+  constexpr int LDK = ChainRec<DK>::LDK, LDC = ChainRec<DK>::LDC, LDT = S::LDT;
+  constexpr int RT = DK / 64;  // update tiles per warp
   extern __shared__ __align__(16) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
-  const int tid = threadIdx.x;
-  const int r = tid >> 2, cg = (tid & 3) * 4;  // token row and first column of this thread
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int fg = lane >> 2, ft = lane & 3;
+  // the 16 x 8 output tile of this warp in the 64 x 16 products: rows 16 rb, columns 8 nt
+  const int rb = warp >> 1, nt = warp & 1;
 
   constexpr int n_tiles = DV / kTile;
   const int tile = blockIdx.x % n_tiles;
@@ -336,7 +387,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
 
   for (int i = tid; i < DK * kTile; i += kThreads) {
     const int d = i / kTile, cc = i % kTile;
-    s.H[i] = p.h0 ? p.h0[hoff + (long long)d * DV + cc] : 0.f;
+    s.H[d * LDT + cc] = p.h0 ? p.h0[hoff + (long long)d * DV + cc] : 0.f;
   }
   if (n_chunks > 0) {
     load_rec<DK, DV, DELTA>(s.rec[0], rec_of(0), tile, tid);
@@ -354,39 +405,68 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
       cp_async_commit();
     }
 
-    // ---- #5 V_new = U - W h   (row r, columns cg..cg+3)
+    // ---- #5 V_new = U - W h   (rows 16 rb.., columns 8 nt..)
     {
-      float4 v = lds4(&b.U[r * kTile + cg]);
-      if (DELTA) {
-        const float4 wh = row_times_tile<DK>(&b.W[r * LDK], s.H, cg);
-        v.x -= wh.x;
-        v.y -= wh.y;
-        v.z -= wh.z;
-        v.w -= wh.w;
+      float acc[4] = {};
+      if (DELTA)
+#pragma unroll
+        for (int k0 = 0; k0 < DK; k0 += 8) {
+          float a[4], bb[2];
+          frag_a(a, b.W, LDK, 16 * rb, k0, fg, ft);
+          frag_b_kn(bb, s.H, LDT, k0, 8 * nt, fg, ft);
+          mma3(acc, a, bb);
+        }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 16 * rb + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
+        s.Vn[r * LDT + cc] = b.U[r * kTile + cc] - acc[i];
       }
-      *reinterpret_cast<float4*>(&s.Vn[r * kTile + cg]) = v;
     }
     __syncthreads();
-    // ---- #6 O = Q~ h + P V_new, and the update's products (h is still the old state)
+    // ---- #6 O = Q~ h + P V_new, and the update's product (h is still the old state)
     {
-      const float4 o1 = row_times_tile<DK>(&b.Qt[r * LDK], s.H, cg);
-      const float4 o2 = row_times_tile<kC>(&b.P[r * LDC], s.Vn, cg);
-      if (r < L)
-        *reinterpret_cast<float4*>(og + (t_seq + (long long)c * kC + r) * v_tok + cg) =
-            make_float4(o1.x + o2.x, o1.y + o2.y, o1.z + o2.z, o1.w + o2.w);
-    }
-    float4 hn[RA];
+      float acc[4] = {};
 #pragma unroll
-    for (int a = 0; a < RA; ++a) hn[a] = row_times_tile<kC>(&b.KtT[(r + 64 * a) * LDC], s.Vn, cg);
+      for (int k0 = 0; k0 < DK; k0 += 8) {
+        float a[4], bb[2];
+        frag_a(a, b.Qt, LDK, 16 * rb, k0, fg, ft);
+        frag_b_kn(bb, s.H, LDT, k0, 8 * nt, fg, ft);
+        mma3(acc, a, bb);
+      }
+#pragma unroll
+      for (int k0 = 0; k0 < kC; k0 += 8) {
+        float a[4], bb[2];
+        frag_a(a, b.P, LDC, 16 * rb, k0, fg, ft);
+        frag_b_kn(bb, s.Vn, LDT, k0, 8 * nt, fg, ft);
+        mma3(acc, a, bb);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = 16 * rb + fg + 8 * h;
+        if (r < L)
+          *reinterpret_cast<float2*>(og + (t_seq + (long long)c * kC + r) * v_tok + 8 * nt + 2 * ft) =
+              make_float2(acc[2 * h], acc[2 * h + 1]);
+      }
+    }
+    float hn[RT][4] = {};
+#pragma unroll
+    for (int a2 = 0; a2 < RT; ++a2)
+#pragma unroll
+      for (int k0 = 0; k0 < kC; k0 += 8) {
+        float a[4], bb[2];
+        frag_a(a, b.KtT, LDC, 16 * rb + 64 * a2, k0, fg, ft);
+        frag_b_kn(bb, s.Vn, LDT, k0, 8 * nt, fg, ft);
+        mma3(hn[a2], a, bb);
+      }
     __syncthreads();  // every read of h and of this chunk's pieces is done
 #pragma unroll
-    for (int a = 0; a < RA; ++a) {
-      float* hp = &s.H[(r + 64 * a) * kTile + cg];
-      const float4 h = lds4(hp);
-      *reinterpret_cast<float4*>(hp) =
-          make_float4(fmaf(gl, h.x, hn[a].x), fmaf(gl, h.y, hn[a].y), fmaf(gl, h.z, hn[a].z),
-                      fmaf(gl, h.w, hn[a].w));
-    }
+    for (int a2 = 0; a2 < RT; ++a2)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int d = 16 * rb + 64 * a2 + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
+        float& hr = s.H[d * LDT + cc];
+        hr = fmaf(gl, hr, hn[a2][i]);
+      }
     if (S::kBufs == 1 && c + 1 < n_chunks) {
       __syncthreads();  // the single buffer is free again
       load_rec<DK, DV, DELTA>(s.rec[0], rec_of(c + 1), tile, tid);
@@ -397,7 +477,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
   if (p.hT) {
     for (int i = tid; i < DK * kTile; i += kThreads) {
       const int d = i / kTile, cc = i % kTile;
-      p.hT[hoff + (long long)d * DV + cc] = s.H[i];
+      p.hT[hoff + (long long)d * DV + cc] = s.H[d * LDT + cc];
     }
   }
 }
