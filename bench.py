@@ -84,7 +84,8 @@ def chain_of(lap, w, choice) -> str:
 
 CHAIN_LABEL = {"tc": "tcgen05, one CTA per chain (state in registers, products in tensor memory)",
                "dv_tile": "mma.sync, one CTA per (chain, dv tile)",
-               "-": "fp32 FMA, one CTA per (chain, 16 dv columns)"}
+               "-": "split-precision tf32 mma.sync (three products per step), one CTA per "
+                    "(chain, 16 dv columns)"}
 
 
 def launches_per_call(w) -> int:
@@ -107,11 +108,11 @@ def measured_traffic(workload: str):
     return rec.get("dram_bytes_per_call")
 
 
-def config_of(w, world, extra=None):
+def config_of(w, world, extra=None, l2_flush="write"):
     cfg = {"workload": w.name, "seqlens": list(w.seqlens) if len(w.seqlens) <= 16 else len(w.seqlens),
            "T_total": w.T_total, "Hqk": w.Hqk, "Hv": w.Hv, "dk": w.dk, "dv": w.dv,
            "chunk": w.chunk, "h0": w.h0_std is not None, "global_batch": w.n_seqs * world,
-           "seq_len": max(w.seqlens), "l2": "flushed (320 MB write) before every timed step",
+           "seq_len": max(w.seqlens), "l2": f"flushed (320 MB {l2_flush}) before every timed step",
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     if extra:
         cfg.update(extra)
@@ -420,6 +421,15 @@ def bench_cuda(args, w, rank, world, local_rank):
     x = make_inputs(w, device=dev, seed=rank_seed(w.seed, rank))
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.l2_flush == "read":  # a reduction over the buffer: L2 left holding clean lines
+        flush.zero_()
+        sink = torch.empty((), dtype=torch.float32, device=dev)
+
+        def flush_l2():
+            torch.sum(flush, dim=0, out=sink)
+    else:
+        def flush_l2():
+            flush.zero_()
     o = torch.empty_like(x["v"])
     hT = torch.empty((w.n_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
 
@@ -435,7 +445,7 @@ def bench_cuda(args, w, rank, world, local_rank):
             scale=w.scale, cu_seqlens=x["cu_seqlens"], stream=stream, **extra)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
@@ -447,7 +457,7 @@ def bench_cuda(args, w, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     for a, b in evs:
-        flush.zero_()
+        flush_l2()
         a.record(stream)
         step()
         b.record(stream)
@@ -469,7 +479,8 @@ def bench_cuda(args, w, rank, world, local_rank):
     host = {k_: (None if x[k_] is None else x[k_].detach().cpu().pin_memory())
             for k_ in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens")}
     pipe = lap.HostPipeline(chunk=w.chunk, device=dev,
-                            op="gdn_prologue" if w.prologue else w.op, depth=2)
+                            op="gdn_prologue" if w.prologue else w.op, depth=2,
+                            scale=w.scale, **extra)
     for _ in range(max(2, args.warmup)):
         pipe.submit(host)
     torch.cuda.synchronize()
@@ -498,7 +509,7 @@ def bench_cuda(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, world, {"chain": CHAIN_LABEL[chain]}),
+        "config": config_of(w, world, {"chain": CHAIN_LABEL[chain]}, args.l2_flush),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic(w.name + (":tc" if chain == "tc" else "")),
@@ -549,6 +560,10 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--ref-step-s", type=float, default=0.5)
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--l2-flush", default="write", choices=["write", "read"],
+                    help="how L2 is flushed before each timed step: writing a 320 MB buffer "
+                         "(default), or reading it, which leaves no dirty lines behind - for DRAM "
+                         "traffic captures with ncu --cache-control none")
     ap.add_argument("--chain", default="auto", choices=["auto", "tc", "dv_tile"],
                     help="chunk-serial kernel of the bf16 forward: the library's own choice "
                          "(default), the tensor-memory chain, or the dv-tile chain")

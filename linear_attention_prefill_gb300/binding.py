@@ -379,14 +379,15 @@ def gdn_device_status(stream=None):
 
 
 def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None, out=None,
-                       op: str = "gdn"):
+                       op: str = "gdn", **fwd_kw):
     """End-to-end call from pinned host memory: copy inputs in, run, copy o and hT out
     (``op`` "ssd" runs ssd_chunk_fwd, "kda" kda_chunk_fwd, "gdn_prologue"
     gdn_chunk_fwd_prologue on raw q, k and gate inputs instead).
 
     ``inputs`` holds pinned CPU tensors q, k, v, g, beta and optionally h0 and
     cu_seqlens.  ``out`` may hold preallocated pinned (o, hT) host tensors and
-    device buffers to reuse.  Returns (o_host, hT_host, bytes_in, bytes_out).
+    device buffers to reuse; ``fwd_kw`` (scale, tc_chain, ...) passes on to the forward.
+    Returns (o_host, hT_host, bytes_in, bytes_out).
     """
     dev = torch.device(device)
     bufs = out.setdefault("dev", {}) if out is not None else {}
@@ -415,7 +416,7 @@ def gdn_chunk_fwd_host(inputs: dict, chunk: int = 64, device="cuda", stream=None
         bufs["workspace"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     o_dev, hT_dev = fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], bufs.get("o"),
                         bufs.get("hT"), chunk=chunk, cu_seqlens=d["cu_seqlens"], stream=stream,
-                        workspace=bufs["workspace"])
+                        workspace=bufs["workspace"], **fwd_kw)
     bufs["o"], bufs["hT"] = o_dev, hT_dev
     if out is not None and "o_host" in out:
         o_h, hT_h = out["o_host"], out["hT_host"]
@@ -439,11 +440,13 @@ class HostPipeline:
     upload of call i + 1 overlaps the compute and the download of call i (the host
     link carries one direction of each at once).  ``submit`` returns the pinned
     (o, hT) of that call and a CUDA event that completes when they are filled.
+    ``fwd_kw`` (scale, tc_chain, ...) passes on to every forward call.
     """
 
-    def __init__(self, chunk: int = 64, device="cuda", op: str = "gdn", depth: int = 2):
+    def __init__(self, chunk: int = 64, device="cuda", op: str = "gdn", depth: int = 2,
+                 **fwd_kw):
         self.dev = torch.device(device)
-        self.chunk, self.op = chunk, op
+        self.chunk, self.op, self.fwd_kw = chunk, op, fwd_kw
         self.slots = [dict(stream=torch.cuda.Stream(self.dev), bufs={}) for _ in range(depth)]
         self.n = 0
 
@@ -454,7 +457,7 @@ class HostPipeline:
         with torch.cuda.stream(slot["stream"]):
             o_h, hT_h, nbytes_in, nbytes_out = gdn_chunk_fwd_host(
                 inputs, chunk=self.chunk, device=self.dev, stream=slot["stream"], out=bufs,
-                op=self.op)
+                op=self.op, **self.fwd_kw)
             done = torch.cuda.Event()
             done.record(slot["stream"])
         return o_h, hT_h, done, nbytes_in, nbytes_out

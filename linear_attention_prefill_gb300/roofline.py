@@ -164,7 +164,15 @@ def traffic_from_ncu_csv(path, launches_per_call):
     return int(sum(per_call) / len(per_call)), kern
 
 
-def write_traffic(csv_path, workload, kernel, launches_per_call, source):
+CACHE_NOTES = {
+    "cold": "ncu flushes L2 before each profiled launch; mean over the profiled calls",
+    "none": "ncu --cache-control none (no flush between the launches of a call); L2 flushed "
+            "by reading a 320 MB buffer before each call (bench.py --l2-flush read); mean over "
+            "the profiled calls",
+}
+
+
+def write_traffic(csv_path, workload, kernel, launches_per_call, source, cache="none"):
     """Record a workload's measured DRAM bytes per call in profiles/traffic.json, stamped
     with the current kernel source hash."""
     per_call, kern = traffic_from_ncu_csv(csv_path, launches_per_call)
@@ -175,8 +183,7 @@ def write_traffic(csv_path, workload, kernel, launches_per_call, source):
         data = {}
     data[workload] = {"kernel": kernel, "kernel_source_hash": kernel_source_hash(),
                       "dram_bytes_per_call": per_call, "kernels": kern,
-                      "cache": "cold: ncu flushes L2 before each profiled launch; mean over "
-                               "the profiled calls", "source": source}
+                      "cache": CACHE_NOTES[cache], "source": source}
     with open(TRAFFIC_JSON, "w") as f:
         json.dump(data, f, indent=1)
     return per_call
@@ -191,5 +198,7 @@ if __name__ == "__main__":
     ap.add_argument("--kernel", required=True, help="what one call launches")
     ap.add_argument("--launches-per-call", type=int, default=2)
     ap.add_argument("--source", default="", help="the profiles/ summary of the capture")
+    ap.add_argument("--cache", default="none", choices=sorted(CACHE_NOTES),
+                    help="how the capture treated L2")
     a = ap.parse_args()
-    print(write_traffic(a.csv, a.workload, a.kernel, a.launches_per_call, a.source))
+    print(write_traffic(a.csv, a.workload, a.kernel, a.launches_per_call, a.source, a.cache))
