@@ -20,8 +20,9 @@
 // accumulation (the split-precision method of Ootomo and Yokota, "Recovering
 // single precision accuracy from Tensor Cores while surpassing the FP32
 // theoretical peak performance", 2022): about 21 significant bits per product,
-// well inside the fp32 path's tolerance.  The triangular solve and the gates stay
-// fp32 on the CUDA cores.
+// well inside the fp32 path's tolerance.  The gates and the solve's four diagonal
+// 16 x 16 blocks stay fp32 on the CUDA cores; the solve's block merges are products
+// like the rest.  Triangular operands are multiplied by their nonzero blocks only.
 //
 // Without the delta rule's erase term (the Mamba-2 scan) A = 0, so Tm = I and the
 // chain takes V_new = U = diag(beta) V.
@@ -54,18 +55,28 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// d += A B for one m16n8k8 step from fp32 fragments (the register layout of the tf32
-// MMA: a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g];
-// d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]; g = lane / 4, t = lane % 4)
-__device__ __forceinline__ void mma3(float (&d)[4], const float (&a)[4], const float (&b)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
+// Fragment layout of the tf32 MMA (g = lane / 4, t = lane % 4): a = A[g][t], A[g+8][t],
+// A[g][t+4], A[g+8][t+4]; b = B[t][g], B[t+4][g]; d = D[g][2t], D[g][2t+1], D[g+8][2t],
+// D[g+8][2t+1].
+// operands split once and reused: hi/lo of an A fragment (4) or a B fragment (2)
+template <int N>
+struct Split {
+  uint32_t h[N], l[N];
+};
+template <int N>
+__device__ __forceinline__ Split<N> split(const float (&x)[N]) {
+  Split<N> r;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
-  mma_tf32(d, al, bh);  // the small terms first
-  mma_tf32(d, ah, bl);
-  mma_tf32(d, ah, bh);
+  for (int i = 0; i < N; ++i) split_tf32(x[i], r.h[i], r.l[i]);
+  return r;
+}
+// d += A_hi B_hi and dx += A_lo B_hi + A_hi B_lo: the big and the small terms in two
+// accumulators, so a k-step adds one MMA to each dependence chain of d and two to dx
+__device__ __forceinline__ void mma3s(float (&d)[4], float (&dx)[4], const Split<4>& a,
+                                      const Split<2>& b) {
+  mma_tf32(dx, a.l, b.h);
+  mma_tf32(dx, a.h, b.l);
+  mma_tf32(d, a.h, b.h);
 }
 // A fragment of rows r0.., columns k0.. of a row-major matrix with row stride ld
 __device__ __forceinline__ void frag_a(float (&a)[4], const float* A, int ld, int r0, int k0,
@@ -113,9 +124,154 @@ struct PrepSmem {
   float V[kC * LDV];
   float A[kC * LDA];  // strictly lower A
   float Tm[kC * LDA];
-  float X[3 * 256];   // solve scratch
+  float X[32 * 40];   // solve scratch: the products Y of the block merges
   float g[kC], beta[kC], G[kC], gam[kC], e[kC];
 };
+
+// The 20 gram tiles on and below the diagonal, 5 per warp j: nA column tiles from ntA
+// in row block rbA, then 5 - nA from ntB in row block rbB.
+struct GramTiles {
+  int rbA, ntA, nA, rbB, ntB;
+};
+__device__ __forceinline__ GramTiles gram_tiles(int j) {
+  switch (j) {
+    case 0: return {0, 0, 2, 3, 0};  // row block 0: 0-1;  row block 3: 0-2
+    case 1: return {1, 0, 4, 3, 3};  // row block 1: 0-3;  row block 3: 3
+    case 2: return {2, 0, 5, 2, 5};  // row block 2: 0-4
+    default: return {2, 5, 1, 3, 4}; // row block 2: 5;    row block 3: 4-7
+  }
+}
+
+// Tm = (I + A)^-1 for the strictly lower 64 x 64 A (row stride LD; only the blocks on
+// and below the diagonal are read), by 16 x 16 blocks: the four diagonal blocks by
+// substitution on the CUDA cores, then two levels of merges on the tensor cores (split
+// tf32).  For a unit lower triangular [[L_a, 0], [A_ba, L_b]] the inverse has the
+// off-diagonal block -L_b^-1 A_ba L_a^-1: level 1 forms it for the 16-row pairs
+// (blocks 1,0 and 3,2), level 2 for the 32-row halves.  X: 32 x 40 floats of scratch.
+template <int LD>
+__device__ __forceinline__ void solve_f32(const float* A, float* T, float* X, int warp, int lane) {
+  const int fg = lane >> 2, ft = lane & 3;
+  if (warp < 4) {
+    if (lane < 16) {  // diagonal block b, column l: once x_m is final it updates every x_i, i > m
+      const int b = warp, l = lane;
+      const float* Ab = A + 16 * b * LD + 16 * b;
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = (i == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m)
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-Ab[i * LD + m], x[m], x[i]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) T[(16 * b + i) * LD + 16 * b + l] = x[i];
+    }
+  } else {
+    for (int e = (warp - 4) * 32 + lane; e < 64 * 16; e += 128) {  // 4-column groups
+      const int r = e >> 4, c = 4 * (e & 15);
+      if ((c >> 4) > (r >> 4))
+        *reinterpret_cast<float4*>(&T[r * LD + c]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __syncthreads();
+  if (warp < 4) {  // level 1: T_IJ = -T_II (A_IJ T_JJ), (I, J) = (1, 0) or (3, 2); 8 columns a warp
+    const int I = 2 * (warp >> 1) + 1, J = I - 1, n0 = 16 * J + 8 * (warp & 1);
+    float y[4] = {}, yx[4] = {};
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+      float a[4], b[2];
+      frag_a(a, A, LD, 16 * I, 16 * J + k0, fg, ft);
+      frag_b_kn(b, T, LD, 16 * J + k0, n0, fg, ft);
+      mma3s(y, yx, split(a), split(b));
+    }
+    float* Y = X + warp * 128;  // 16 x 8, row stride 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Y[(fg + 8 * (i >> 1)) * 8 + 2 * ft + (i & 1)] = y[i] + yx[i];
+    __syncwarp();
+    float t[4] = {}, tx[4] = {};
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+      float a[4], b[2];
+      frag_a(a, T, LD, 16 * I, 16 * I + k0, fg, ft);
+      frag_b_kn(b, Y, 8, k0, 0, fg, ft);
+      mma3s(t, tx, split(a), split(b));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      T[(16 * I + fg + 8 * (i >> 1)) * LD + n0 + 2 * ft + (i & 1)] = -(t[i] + tx[i]);
+  }
+  __syncthreads();
+  // level 2: rows 32-63 x columns 0-31 = -T_bb (A_ba T_aa); warp: 16 rows rb, 8 columns n0
+  const int rb = warp >> 2, n0 = 8 * (warp & 3);
+  {
+    float y[4] = {}, yx[4] = {};
+    for (int k0 = n0; k0 < 32; k0 += 8) {  // T_aa[k][n] = 0 for k < n
+      float a[4], b[2];
+      frag_a(a, A, LD, 32 + 16 * rb, k0, fg, ft);
+      frag_b_kn(b, T, LD, k0, n0, fg, ft);
+      mma3s(y, yx, split(a), split(b));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[(16 * rb + fg + 8 * (i >> 1)) * 40 + n0 + 2 * ft + (i & 1)] = y[i] + yx[i];
+  }
+  __syncthreads();
+  {
+    float t[4] = {}, tx[4] = {};
+    for (int k0 = 0; k0 < 16 * (rb + 1); k0 += 8) {  // T_bb[r][k] = 0 for k > r
+      float a[4], b[2];
+      frag_a(a, T, LD, 32 + 16 * rb, 32 + k0, fg, ft);
+      frag_b_kn(b, X, 40, k0, n0, fg, ft);
+      mma3s(t, tx, split(a), split(b));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      T[(32 + 16 * rb + fg + 8 * (i >> 1)) * LD + n0 + 2 * ft + (i & 1)] = -(t[i] + tx[i]);
+  }
+  __syncthreads();
+}
+
+// One of the prep's products out = Tm diag(f) B for a [64][N] operand B (row stride LDB)
+// with f = beta gamma (gam given) or beta: this warp's column tiles of row blocks rbs[0]
+// and rbs[1], N / 32 tiles of 8 columns each, in half `half` of the columns; out is
+// row-major [64][N].
+template <int N, int LDB>
+__device__ __forceinline__ void wu_product(const float* Tm, int lda, const float* B,
+                                           const float* beta, const float* gam,
+                                           const int (&rbs)[2], int half, float* out, int fg,
+                                           int ft) {
+  constexpr int NQ = N / 32;
+  float acc[2][NQ][4] = {}, accx[2][NQ][4] = {};
+#pragma unroll
+  for (int k0 = 0; k0 < kC; k0 += 8) {
+    const float f0 = gam ? beta[k0 + ft] * gam[k0 + ft] : beta[k0 + ft];
+    const float f1 = gam ? beta[k0 + ft + 4] * gam[k0 + ft + 4] : beta[k0 + ft + 4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (k0 >= 16 * (rbs[u] + 1)) continue;  // above the diagonal block
+      float a[4];
+      frag_a(a, Tm, lda, 16 * rbs[u], k0, fg, ft);
+      const Split<4> sa = split(a);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        float b[2];
+        frag_b_kn(b, B, LDB, k0, half * (N / 2) + 8 * (u * NQ + q), fg, ft);
+        b[0] *= f0;
+        b[1] *= f1;
+        mma3s(acc[u][q], accx[u][q], sa, split(b));
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = 16 * rbs[u] + fg + 8 * h, cc = half * (N / 2) + 8 * (u * NQ + q) + 2 * ft;
+        *reinterpret_cast<float2*>(&out[r * N + cc]) =
+            make_float2(acc[u][q][2 * h] + accx[u][q][2 * h],
+                        acc[u][q][2 * h + 1] + accx[u][q][2 * h + 1]);
+      }
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams p, const WsLayout ws) {
@@ -207,106 +363,81 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
   }
   __syncthreads();
 
-  // ---- #2 KK^T and QK^T: warp w takes rows 16 (w % 4) of K (w < 4) or of Q (w >= 4)
-  // against all 64 keys: 8 n-tiles of 8 columns, DK / 8 k-steps
+  // ---- #2 KK^T and QK^T (warps 0-3: K rows, warps 4-7: Q rows).  Both grams are
+  // needed on and below the diagonal only: of the 4 x 8 tiles (16 rows x 8 columns) the
+  // 20 with columns below 16 (rb + 1) are formed, 5 per warp, a warp taking the tiles
+  // of one or two row blocks (gram_tiles)
   {
     const bool isQ = warp >= 4;
-    const int r0 = 16 * (warp & 3);
+    const int j = warp & 3;
+    const GramTiles gt = gram_tiles(j);
+    const int rbA = gt.rbA, ntA = gt.ntA, nA = gt.nA, rbB = gt.rbB, ntB = gt.ntB;
     const float* Arows = isQ ? s.Q : s.K;
-    float acc[8][4] = {};
-#pragma unroll
+    float acc[5][4] = {}, accx[5][4] = {};
+#pragma unroll 2
     for (int k0 = 0; k0 < DK; k0 += 8) {
       float a[4];
-      frag_a(a, Arows, LDK, r0, k0, fg, ft);
+      frag_a(a, Arows, LDK, 16 * rbA, k0, fg, ft);
+      const Split<4> sa = split(a);
+      frag_a(a, Arows, LDK, 16 * rbB, k0, fg, ft);
+      const Split<4> sb = split(a);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int t = 0; t < 5; ++t) {
+        const bool inA = t < nA;
         float b[2];
-        frag_b_nk(b, s.K, LDK, k0, 8 * nt, fg, ft);
-        mma3(acc[nt], a, b);
+        frag_b_nk(b, s.K, LDK, k0, 8 * (inA ? ntA + t : ntB + t - nA), fg, ft);
+        mma3s(acc[t], accx[t], inA ? sa : sb, split(b));
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int t = 0; t < 5; ++t) {
+      const bool inA = t < nA;
+      const int rb = inA ? rbA : rbB, nt = inA ? ntA + t : ntB + t - nA;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = r0 + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
+        const int r = 16 * rb + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
+        const float x = acc[t][i] + accx[t][i];
         const bool low = r >= cc && r < L;
         const float m = low ? expf(s.G[r] - s.G[cc]) : 0.f;
         if (isQ)
-          rec[R::P + r * kC + cc] = low ? p.scale * m * acc[nt][i] : 0.f;
+          rec[R::P + r * kC + cc] = low ? p.scale * m * x : 0.f;
         else
-          s.A[r * LDA + cc] = (low && r > cc && delta) ? s.beta[r] * m * acc[nt][i] : 0.f;
+          s.A[r * LDA + cc] = (low && r > cc && delta) ? s.beta[r] * m * x : 0.f;
       }
+    }
   }
-  // Kt^T and Q~ go out while the others finish the grams
-  for (int i = tid; i < kC * DK; i += kThreads) {
-    const int r = i / DK, d = i % DK;  // token r, channel d
-    rec[R::Qt + r * DK + d] = p.scale * s.gam[r] * s.Q[r * LDK + d];
-    const int dd = i / kC, j = i % kC;  // channel dd, token j: coalesced transposed store
-    rec[R::KtT + dd * kC + j] = s.e[j] * s.K[j * LDK + dd];
+  // P above the formed tiles is zero (the chain reads P whole); A there is never read
+  for (int i = tid; i < kC * kC / 4; i += kThreads) {
+    const int r = (4 * i) / kC, cc = (4 * i) % kC;
+    if (cc >= 16 * ((r >> 4) + 1))
+      *reinterpret_cast<float4*>(&rec[R::P + r * kC + cc]) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // Q~ and Kt^T go out while the others finish the grams, 16 bytes a store
+  for (int i = tid; i < kC * DK / 4; i += kThreads) {
+    const int r = (4 * i) / DK, d = (4 * i) % DK;  // token r, channels d..d+3
+    const float f = p.scale * s.gam[r];
+    const float4 x = *reinterpret_cast<const float4*>(&s.Q[r * LDK + d]);
+    *reinterpret_cast<float4*>(&rec[R::Qt + r * DK + d]) =
+        make_float4(f * x.x, f * x.y, f * x.z, f * x.w);
+    const int dd = i % DK, j = 4 * (i / DK);  // channel dd, tokens j..j+3
+    *reinterpret_cast<float4*>(&rec[R::KtT + dd * kC + j]) =
+        make_float4(s.e[j] * s.K[j * LDK + dd], s.e[j + 1] * s.K[(j + 1) * LDK + dd],
+                    s.e[j + 2] * s.K[(j + 2) * LDK + dd], s.e[j + 3] * s.K[(j + 3) * LDK + dd]);
   }
   __syncthreads();
 
-  // ---- #3 Solve: Tm = (I + A)^-1 (fp32, CUDA cores)
-  solve_unit_lower_64_f32<kThreads>(s.A, LDA, s.Tm, LDA, s.X);
+  // ---- #3 Solve: Tm = (I + A)^-1
+  solve_f32<LDA>(s.A, s.Tm, s.X, warp, lane);
 
-  // ---- #4 W = Tm diag(beta gamma) K, U = Tm diag(beta) V: warp w takes rows 16 (w % 4)
-  // and half w / 4 of the columns
+  // ---- #4 W = Tm diag(beta gamma) K, U = Tm diag(beta) V.  Tm is lower triangular, so
+  // row block rb needs the k-steps up to 2 rb + 1 only; warp w pairs row blocks j = w % 4
+  // and 3 - j (10 k-steps of work per column tile either way) over a quarter of the
+  // columns of half w / 4 each
   {
-    const int r0 = 16 * (warp & 3), half = warp >> 2;
-    if (delta) {
-      constexpr int NT = DK / 16;  // n-tiles in a half
-      float acc[NT][4] = {};
-#pragma unroll
-      for (int k0 = 0; k0 < kC; k0 += 8) {
-        float a[4];
-        frag_a(a, s.Tm, LDA, r0, k0, fg, ft);
-        const float f0 = s.beta[k0 + ft] * s.gam[k0 + ft];
-        const float f1 = s.beta[k0 + ft + 4] * s.gam[k0 + ft + 4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float b[2];
-          frag_b_kn(b, s.K, LDK, k0, half * (DK / 2) + 8 * nt, fg, ft);
-          b[0] *= f0;
-          b[1] *= f1;
-          mma3(acc[nt], a, b);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = r0 + fg + 8 * h, cc = half * (DK / 2) + 8 * nt + 2 * ft;
-          *reinterpret_cast<float2*>(&rec[R::W + r * DK + cc]) =
-              make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-        }
-    }
-    {
-      constexpr int NT = DV / 16;
-      float acc[NT][4] = {};
-#pragma unroll
-      for (int k0 = 0; k0 < kC; k0 += 8) {
-        float a[4];
-        frag_a(a, s.Tm, LDA, r0, k0, fg, ft);
-        const float f0 = s.beta[k0 + ft], f1 = s.beta[k0 + ft + 4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float b[2];
-          frag_b_kn(b, s.V, LDV, k0, half * (DV / 2) + 8 * nt, fg, ft);
-          b[0] *= f0;
-          b[1] *= f1;
-          mma3(acc[nt], a, b);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = r0 + fg + 8 * h, cc = half * (DV / 2) + 8 * nt + 2 * ft;
-          *reinterpret_cast<float2*>(&rec[R::U + r * DV + cc]) =
-              make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
-        }
-    }
+    const int j = warp & 3, half = warp >> 2;
+    const int rbs[2] = {j, 3 - j};
+    if (delta) wu_product<DK, LDK>(s.Tm, LDA, s.K, s.beta, s.gam, rbs, half, rec + R::W, fg, ft);
+    wu_product<DV, LDV>(s.Tm, LDA, s.V, s.beta, nullptr, rbs, half, rec + R::U, fg, ft);
   }
 }
 
@@ -405,59 +536,56 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
       cp_async_commit();
     }
 
-    // ---- #5 V_new = U - W h   (rows 16 rb.., columns 8 nt..)
+    // ---- #5 V_new = U - W h and the Q~ h half of #6 O, both from the old state
+    // (rows 16 rb.., columns 8 nt..; each split B fragment of h serves both)
+    float ao[4] = {}, aox[4] = {};
     {
-      float acc[4] = {};
-      if (DELTA)
-#pragma unroll
-        for (int k0 = 0; k0 < DK; k0 += 8) {
-          float a[4], bb[2];
+      float av[4] = {}, avx[4] = {};
+#pragma unroll 4
+      for (int k0 = 0; k0 < DK; k0 += 8) {
+        float a[4], bb[2];
+        frag_b_kn(bb, s.H, LDT, k0, 8 * nt, fg, ft);
+        const Split<2> sb = split(bb);
+        if (DELTA) {
           frag_a(a, b.W, LDK, 16 * rb, k0, fg, ft);
-          frag_b_kn(bb, s.H, LDT, k0, 8 * nt, fg, ft);
-          mma3(acc, a, bb);
+          mma3s(av, avx, split(a), sb);
         }
+        frag_a(a, b.Qt, LDK, 16 * rb, k0, fg, ft);
+        mma3s(ao, aox, split(a), sb);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = 16 * rb + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
-        s.Vn[r * LDT + cc] = b.U[r * kTile + cc] - acc[i];
+        s.Vn[r * LDT + cc] = b.U[r * kTile + cc] - (av[i] + avx[i]);
       }
     }
     __syncthreads();
-    // ---- #6 O = Q~ h + P V_new, and the update's product (h is still the old state)
-    {
-      float acc[4] = {};
-#pragma unroll
-      for (int k0 = 0; k0 < DK; k0 += 8) {
-        float a[4], bb[2];
-        frag_a(a, b.Qt, LDK, 16 * rb, k0, fg, ft);
-        frag_b_kn(bb, s.H, LDT, k0, 8 * nt, fg, ft);
-        mma3(acc, a, bb);
-      }
-#pragma unroll
-      for (int k0 = 0; k0 < kC; k0 += 8) {
-        float a[4], bb[2];
+    // ---- #6 O += P V_new (P is zero right of the diagonal block) and the update's
+    // product Kt^T V_new (h is still the old state); each split B fragment of V_new
+    // serves both
+    float hn[RT][4] = {}, hnx[RT][4] = {};
+#pragma unroll 2
+    for (int k0 = 0; k0 < kC; k0 += 8) {
+      float a[4], bb[2];
+      frag_b_kn(bb, s.Vn, LDT, k0, 8 * nt, fg, ft);
+      const Split<2> sb = split(bb);
+      if (k0 < 16 * (rb + 1)) {
         frag_a(a, b.P, LDC, 16 * rb, k0, fg, ft);
-        frag_b_kn(bb, s.Vn, LDT, k0, 8 * nt, fg, ft);
-        mma3(acc, a, bb);
+        mma3s(ao, aox, split(a), sb);
       }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = 16 * rb + fg + 8 * h;
-        if (r < L)
-          *reinterpret_cast<float2*>(og + (t_seq + (long long)c * kC + r) * v_tok + 8 * nt + 2 * ft) =
-              make_float2(acc[2 * h], acc[2 * h + 1]);
+      for (int a2 = 0; a2 < RT; ++a2) {
+        frag_a(a, b.KtT, LDC, 16 * rb + 64 * a2, k0, fg, ft);
+        mma3s(hn[a2], hnx[a2], split(a), sb);
       }
     }
-    float hn[RT][4] = {};
 #pragma unroll
-    for (int a2 = 0; a2 < RT; ++a2)
-#pragma unroll
-      for (int k0 = 0; k0 < kC; k0 += 8) {
-        float a[4], bb[2];
-        frag_a(a, b.KtT, LDC, 16 * rb + 64 * a2, k0, fg, ft);
-        frag_b_kn(bb, s.Vn, LDT, k0, 8 * nt, fg, ft);
-        mma3(hn[a2], a, bb);
-      }
+    for (int h = 0; h < 2; ++h) {
+      const int r = 16 * rb + fg + 8 * h;
+      if (r < L)
+        *reinterpret_cast<float2*>(og + (t_seq + (long long)c * kC + r) * v_tok + 8 * nt + 2 * ft) =
+            make_float2(ao[2 * h] + aox[2 * h], ao[2 * h + 1] + aox[2 * h + 1]);
+    }
     __syncthreads();  // every read of h and of this chunk's pieces is done
 #pragma unroll
     for (int a2 = 0; a2 < RT; ++a2)
@@ -465,7 +593,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
       for (int i = 0; i < 4; ++i) {
         const int d = 16 * rb + 64 * a2 + fg + 8 * (i >> 1), cc = 8 * nt + 2 * ft + (i & 1);
         float& hr = s.H[d * LDT + cc];
-        hr = fmaf(gl, hr, hn[a2][i]);
+        hr = fmaf(gl, hr, hn[a2][i] + hnx[a2][i]);
       }
     if (S::kBufs == 1 && c + 1 < n_chunks) {
       __syncthreads();  // the single buffer is free again
