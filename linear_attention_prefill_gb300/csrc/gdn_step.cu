@@ -38,6 +38,15 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
   const int hq = qk_head(hv, p.Hqk, p.Hv, p.head_map);
   const TIn* q = static_cast<const TIn*>(p.q) + ((long long)n * p.Hqk + hq) * DK;
   const TIn* k = static_cast<const TIn*>(p.k) + ((long long)n * p.Hqk + hq) * DK;
+  const long long nh = (long long)n * p.Hv + hv;
+  const int col = tile * kCols + lane;
+  // the state tile is requested first: its loads are in flight while k, q and the
+  // gates arrive (rows warp + 4 i of column col)
+  constexpr int R = DK / kWarps;  // rows per thread
+  float* h = p.h + nh * DK * p.dv + col;
+  float hr[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) hr[i] = h[(long long)(warp + kWarps * i) * p.dv];
   for (int i = tid; i < DK; i += kWarps * 32) {
     sk[i] = to_f(k[i]);
     sq[i] = to_f(q[i]);
@@ -70,7 +79,6 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
     sk[i] *= rk;
     sq[i] *= rq * p.scale;
   }
-  const long long nh = (long long)n * p.Hv + hv;
   float gate = p.kda ? 0.f : p.g[nh], b = p.beta[nh];
   if (p.prologue) {  // raw gates: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
     const float x = gate + (p.dt_bias ? p.dt_bias[hv] : 0.f);
@@ -80,18 +88,14 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_step_kernel(const StepParams 
   const float alpha = p.kda ? 0.f : expf(gate);
   if (p.kda)  // Kimi Delta Attention: row r of h decays by exp(g[r])
     for (int i = tid; i < DK; i += kWarps * 32) sa[i] = expf(p.g[nh * DK + i]);
-  const int col = tile * kCols + lane;
   const float vcol = to_f(static_cast<const TIn*>(p.v)[nh * p.dv + col]);
   __syncthreads();
 
-  constexpr int R = DK / kWarps;  // rows per thread
-  float* h = p.h + nh * DK * p.dv + col;
-  float hr[R];
   float part = 0.f;
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int r = warp + kWarps * i;
-    hr[i] = (p.kda ? sa[r] : alpha) * h[(long long)r * p.dv];
+    hr[i] *= p.kda ? sa[r] : alpha;
     part += hr[i] * sk[r];
   }
   red1[warp][lane] = part;
