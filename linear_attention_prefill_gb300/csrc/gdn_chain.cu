@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ======================= producer ======================================
     if (lane == 0) {
+      griddep_wait();  // the records are the prep launch's output
       auto issue = [&](int c) {
         unsigned char* st = sm + (c % kStages) * Lo::kStageBytes;
         uint64_t* bar = &full[c % kStages];
@@ -393,24 +394,24 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
     cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, 64, false, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L64::kAlloc);
     if (e != cudaSuccess) return e;
-    gdn_chain_kernel<DK, 64, false, true><<<(unsigned)grid, kThreads, L64::kAlloc, stream>>>(p, ws);
-    return cudaGetLastError();
+    return launch_after(gdn_chain_kernel<DK, 64, false, true>, (unsigned)grid, kThreads,
+                        L64::kAlloc, stream, p, ws);
   } else {
     if (p.kda) {  // KDA records exist for dk = 128 only
       if constexpr (DK == 128) {
         cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
         if (e != cudaSuccess) return e;
-        gdn_chain_kernel<DK, DVT, true><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
-        return cudaGetLastError();
+        return launch_after(gdn_chain_kernel<DK, DVT, true>, (unsigned)grid, kThreads, Lo::kAlloc,
+                            stream, p, ws);
       }
       return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(gdn_chain_kernel<DK, DVT, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
     if (e != cudaSuccess) return e;
-    gdn_chain_kernel<DK, DVT, false><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws);
-    return cudaGetLastError();
+    return launch_after(gdn_chain_kernel<DK, DVT, false>, (unsigned)grid, kThreads, Lo::kAlloc,
+                        stream, p, ws);
   }
 }
 

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stage jj holds chunk jj-1's Q~, Kt, P^T (jj >= 1) and chunk jj's W', X^T, U^T,
       // gates (jj < n_chunks): everything step jj-1 and the V / state epilogues after
       // it read.  The prologue reads stage 0.
+      griddep_wait();  // the records are the prep launch's output
       int issued = 0;
       for (int jj = 0; jj <= n_chunks; ++jj) {
         const int s = jj % kStages;
@@ -565,8 +566,8 @@ cudaError_t launch_t(const FwdParams& p, const WsLayout& ws, cudaStream_t stream
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Lo::kAlloc);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.N * p.Hv;
-  gdn_chain_tc_kernel<DK, DV, DELTA><<<(unsigned)grid, kThreads, Lo::kAlloc, stream>>>(p, ws, mo);
-  return cudaGetLastError();
+  return launch_after(gdn_chain_tc_kernel<DK, DV, DELTA>, (unsigned)grid, kThreads, Lo::kAlloc,
+                      stream, p, ws, mo);
 }
 
 template <int DK, int DV>

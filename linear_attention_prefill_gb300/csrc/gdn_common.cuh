@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 // Optional phase timing (compile with -DGDN_PROFILE): thread 0 of every CTA adds
 // the clock64() cycles spent since the previous mark to g_gdn_phase[id].  Off in
 // the library build, where the marks compile to nothing.
@@ -129,6 +131,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
 }
 // global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned;
 // completion is counted on `bar` (its transaction count must expect the bytes).
+// Programmatic dependent launch: a kernel lets the next launch on its stream (made with
+// launch_after) start early; that kernel's griddep_wait() returns once this grid has
+// completed and its memory operations are visible.  Both are no-ops otherwise.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, unsigned bytes,
                                          uint64_t* bar) {
   asm volatile(
@@ -361,6 +371,25 @@ __device__ __forceinline__ void solve_unit_lower_64_f32(const float* A, int lda,
     }
     __syncthreads();
   }
+}
+
+// Launch `kernel` as a programmatic dependent of the previous work on `stream`: its
+// CTAs may become resident before that work completes, and must call griddep_wait()
+// before reading anything it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                         cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace gdn

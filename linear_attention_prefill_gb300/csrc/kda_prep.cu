@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, 2) kda_prep_kernel(const FwdParams p
   const int hv = blockIdx.x % p.Hv;
   const long long slot = blockIdx.x / p.Hv;
   int n, c;
+  // the chain launch may come in now: it waits for this grid before reading a record
+  griddep_launch_dependents();
   if (!locate_chunk(p, ws, slot, &n, &c)) return;
   const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
   const long long len =
