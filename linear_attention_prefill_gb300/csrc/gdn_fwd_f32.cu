@@ -286,6 +286,8 @@ __global__ void __launch_bounds__(kThreads) gdn_prep_f32_kernel(const FwdParams 
   const int hv = blockIdx.x % p.Hv;
   const long long slot = blockIdx.x / p.Hv;
   int n, c;
+  // the chain launch may come in now: it waits for this grid before reading a record
+  griddep_launch_dependents();
   if (!locate_chunk(p, ws, slot, &n, &c)) return;
   const long long t_seq = p.cu_seqlens ? (long long)p.cu_seqlens[n] : (long long)n * p.T;
   const long long len = p.cu_seqlens ? (long long)p.cu_seqlens[n + 1] - t_seq : (long long)p.T;
@@ -520,6 +522,7 @@ __global__ void __launch_bounds__(kThreads) gdn_chain_f32_kernel(const FwdParams
     const int d = i / kTile, cc = i % kTile;
     s.H[d * LDT + cc] = p.h0 ? p.h0[hoff + (long long)d * DV + cc] : 0.f;
   }
+  griddep_wait();  // the records are the prep launch's output
   if (n_chunks > 0) {
     load_rec<DK, DV, DELTA>(s.rec[0], rec_of(0), tile, tid);
     cp_async_commit();
@@ -624,14 +627,14 @@ cudaError_t launch_dd(const FwdParams& p, const WsLayout& ws, cudaStream_t strea
     e = cudaFuncSetAttribute(gdn_chain_f32_kernel<DK, DV, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
     if (e != cudaSuccess) return e;
-    gdn_chain_f32_kernel<DK, DV, true><<<grid, kThreads, sc, stream>>>(p, ws);
+    e = launch_after(gdn_chain_f32_kernel<DK, DV, true>, grid, kThreads, sc, stream, p, ws);
   } else {
     e = cudaFuncSetAttribute(gdn_chain_f32_kernel<DK, DV, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
     if (e != cudaSuccess) return e;
-    gdn_chain_f32_kernel<DK, DV, false><<<grid, kThreads, sc, stream>>>(p, ws);
+    e = launch_after(gdn_chain_f32_kernel<DK, DV, false>, grid, kThreads, sc, stream, p, ws);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <int DK, int DV>
