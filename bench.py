@@ -438,7 +438,9 @@ def bench_cuda(args, w, rank, world, local_rank):
         def fwd(q, k, v, a, b, h0, o, hT, **kw):
             return lap.gdn_chunk_fwd_prologue(q, k, v, a, b, None, None, h0, o, hT, **kw)
     chain = chain_of(lap, w, args.chain)
-    extra = {} if w.dtype == "f32" or args.chain == "auto" else {"tc_chain": args.chain == "tc"}
+    # fp32 and KDA have one chain each (config.chain names the one that ran)
+    extra = ({} if w.dtype == "f32" or w.op == "kda" or args.chain == "auto"
+             else {"tc_chain": args.chain == "tc"})
 
     def step():
         fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT, chunk=w.chunk,
