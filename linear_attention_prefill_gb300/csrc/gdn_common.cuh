@@ -93,12 +93,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
-// Count `bytes` of the current phase's expected transactions as done, without
-// any copy (releases a barrier whose copy was not issued).
-__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, unsigned bytes) {
-  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
 // Arrive once and add `bytes` to the transaction count of the current phase.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
@@ -152,12 +146,6 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
           smem_u32(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-// shared -> global, same size and alignment rules; tracked by bulk_commit/bulk_wait.
-__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, unsigned bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gmem_dst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Wait until at most N committed bulk stores still read their shared source.
@@ -294,19 +282,6 @@ __device__ __forceinline__ void bf16x8_to_f16x8(void* p) {
   *reinterpret_cast<uint4*>(p) = out;
 }
 
-// As bf16x8_to_f16x8, each value multiplied by `scale` in fp32 before rounding.
-__device__ __forceinline__ void bf16x8_to_f16x8_scaled(void* p, float scale) {
-  uint4 raw = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
-  uint4 out;
-  __half2* h = reinterpret_cast<__half2*>(&out);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(b[i]);
-    h[i] = __floats2half2_rn(f.x * scale, f.y * scale);
-  }
-  *reinterpret_cast<uint4*>(p) = out;
-}
 
 // Non-zero if either fp16 half of `w` is an infinity or a NaN (exponent field all
 // ones): adding 1 to a full 5-bit exponent field carries into the half's sign bit.
@@ -322,62 +297,6 @@ __device__ __forceinline__ void c_to_a(uint32_t (&a)[4], const float (&c0)[4], c
   a[3] = pack_f16(c1[2], c1[3]);
 }
 
-// ---- blocked unit-lower-triangular inverse, 64 x 64, all fp32 (SIMT) -----------
-// T = (I + A)^-1 for strictly lower-triangular A, every product in fp32 on the
-// CUDA cores, for the fp32 path: diagonal 16x16 blocks by forward substitution
-// (x_i = [i == l] - sum_{m<i} A_im x_m), then block row by block row
-// T_IJ = -T_II * sum_{J<=M<I} A_IM T_MJ.  Called by all NTHREADS
-// (>= 256) threads; X is 3*256 floats of scratch; ends with a barrier.
-template <int NTHREADS>
-__device__ __forceinline__ void solve_unit_lower_64_f32(const float* A, int lda, float* T, int ldt,
-                                                        float* X) {
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  static_assert(NTHREADS >= 256, "solve needs 8 warps");
-  if (warp < 4 && lane < 16) {
-    const int b = warp, l = lane;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s = (i == l) ? 1.f : 0.f;
-#pragma unroll
-      for (int m = 0; m < i; ++m) s -= A[(16 * b + i) * lda + 16 * b + m] * x[m];
-      x[i] = s;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) T[(16 * b + i) * ldt + 16 * b + l] = x[i];
-  } else if (warp >= 4) {
-    for (int e = tid - 128; e < 64 * 64; e += NTHREADS - 128) {
-      const int r = e >> 6, c = e & 63;
-      if ((c >> 4) > (r >> 4)) T[r * ldt + c] = 0.f;
-    }
-  }
-  __syncthreads();
-  for (int I = 1; I < 4; ++I) {
-    for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      float s = 0.f;
-      for (int M = J; M < I; ++M) {
-        const float* arow = A + (16 * I + r) * lda + 16 * M;
-        const float* tcol = T + (16 * M) * ldt + 16 * J + c;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) s += arow[m] * tcol[m * ldt];
-      }
-      X[e] = s;
-    }
-    __syncthreads();
-    for (int e = tid; e < I * 256; e += NTHREADS) {
-      const int J = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const float* trow = T + (16 * I + r) * ldt + 16 * I;
-      const float* xc = X + J * 256 + c;
-      float s = 0.f;
-#pragma unroll
-      for (int m = 0; m <= r; ++m) s += trow[m] * xc[m * 16];
-      T[(16 * I + r) * ldt + 16 * J + c] = -s;
-    }
-    __syncthreads();
-  }
-}
 
 // Launch `kernel` as a programmatic dependent of the previous work on `stream`: its
 // CTAs may become resident before that work completes, and must call griddep_wait()
