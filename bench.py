@@ -55,6 +55,7 @@ L2_FLUSH_BYTES = 320 * 2 ** 20
 # alike.  The roofline block times the call, and the launch list in profiles/ gives
 # each kernel's share.
 KERNEL_NAME = "gdn_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel)"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the roofline's)
 KERNEL_NAMES = {"ssd": "ssd_chunk_fwd (gdn_prep_kernel + gdn_chain_kernel, no erase term)",
                 "kda": "kda_chunk_fwd (kda_prep_kernel + gdn_chain_kernel in KDA mode)",
                 "gdn_prologue": "gdn_chunk_fwd_prologue (gdn_prep_kernel with the fused prologue + "
@@ -516,6 +517,7 @@ def bench_cuda(args, w, rank, world, local_rank):
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic(w.name + (":tc" if chain == "tc" else "")),
                      "peak_source": src,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": kernel_name(w, chain),
                      "algorithmic_bytes": model["bytes"],
                      "algorithmic_flops": model["flops"],

@@ -52,6 +52,7 @@ def test_cuda_arm_line(workload, launches):
     assert r["bound"] in ("hbm", "tensor", "alu") and r["unit"] in ("GB/s", "TFLOP/s")
     assert r["peak"] > 0 and r["achieved"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert 0 < r["frac_of_nominal"] <= r["frac"]  # the nominal 7.9 TB/s is above the measured peak
     assert r["traffic"] is None or r["traffic"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
