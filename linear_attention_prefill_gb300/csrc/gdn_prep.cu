@@ -60,11 +60,11 @@ struct PrepLayout {
   static constexpr int kTw = kAfterTh + (kVinQ ? 0 : (DV / 64) * 8192);  // bf16 [64][64] sw128
   static constexpr int kTu = kTw + 8192;                                   // fp16 [64][64] sw128
   static constexpr int kAd = kTu + 8192;               // fp32 diagonal blocks of A [4][16][16]
-  static constexpr int kVec = kAd + 4 * 256 * 4;  // beta, G, gamma, e, beta*gamma, 1/|k|, 1/|q|
+  static constexpr int kVec = kAd + 4 * 256 * 4;  // beta, G (log2 units), gamma, e, beta*gamma, 1/|k|, 1/|q|
   static constexpr int kBar = kVec + 7 * kC * 4;  // 5 mbarriers, tmem address, abort flag
   static constexpr int kBytes = kBar + 64;
   static constexpr int kAlloc = kBytes + 1024;         // slack to align the base
-  static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kAd % 16 == 0, "alignment");
+  static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kAd % 16 == 0 && kVec % 16 == 0, "alignment");
 };
 
 // 8 bf16 values at p (16-byte aligned) times `scale`, rounded once to fp16.
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     const float Glast = __shfl_sync(0xffffffffu, incl, 31);
     const float G0 = incl - g1, G1 = incl;
     const float gam0 = expf(G0), gam1 = expf(G1);
-    s_G[r0] = G0;
-    s_G[r1] = G1;
+    s_G[r0] = G0 * kLog2e;  // log2 units: the masks' exponent
+    s_G[r1] = G1 * kLog2e;
     s_gam[r0] = gam0;
     s_gam[r1] = gam1;
     s_e[r0] = expf(Glast - G0);
@@ -313,15 +313,11 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int r = R & (kC - 1), c0 = 32 * h;
     float x[32];
     tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + c0, x);
-    const float Gr = s_G[r], rowf = isP ? p.scale * s_rq[r] : s_beta[r] * s_rk[r];
+    const float rowf = isP ? p.scale * s_rq[r] : s_beta[r] * s_rk[r];
     // last column kept; without the erase term (SSD) A is zero, so Tm = I and U = diag(beta) V
     const int lim = isP ? r : (p.delta_rule ? r - 1 : -1);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int cc = c0 + j;
-      const float m = ex2_approx((Gr - s_G[cc]) * kLog2e);
-      x[j] = (cc <= lim && r < L) ? rowf * m * s_rk[cc] * x[j] : 0.f;
-    }
+    if (p.prologue) mask_row32<true>(x, s_G, s_rk, c0, s_G[r], rowf, lim, r < L);
+    else mask_row32<false>(x, s_G, nullptr, c0, s_G[r], rowf, lim, r < L);
     if (isP) {
       __half* P = ws.P(slot, hv, p.Hv);
 #pragma unroll

@@ -70,7 +70,8 @@ struct PrepLayout {
   static constexpr int kBar = kVec + 8 * kC * 4;  // 7 mbarriers, tmem address, flags
   static constexpr int kBytes = kBar + 128;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base
-  static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kY % 1024 == 0 && kAd % 16 == 0,
+  static_assert(kTw % 1024 == 0 && kTh % 1024 == 0 && kY % 1024 == 0 && kAd % 16 == 0 &&
+                kVec % 16 == 0,
                 "alignment");
 };
 
@@ -250,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     const float Glast = __shfl_sync(0xffffffffu, incl, 31);
     const float G0 = incl - g1, G1 = incl;
     const float gam0 = expf(G0), gam1 = expf(G1);
-    s_G[r0] = G0;
-    s_G[r1] = G1;
+    s_G[r0] = G0 * kLog2e;  // log2 units: the masks' exponent
+    s_G[r1] = G1 * kLog2e;
     s_gam[r0] = gam0;
     s_gam[r1] = gam1;
     s_e[r0] = expf(Glast - G0);
@@ -397,16 +398,11 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int r = R & (kC - 1), c0 = 32 * h;
     float x[32];
     tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + c0, x);
-    const float Gr = s_G[r];
+    const float rowf = isP ? p.scale * s_rq[r] : s_beta[r] * s_rk[r];
     // last column kept; without the erase term (SSD) A is zero, so Tm = I and U = diag(beta) V
     const int lim = isP ? r : (delta ? r - 1 : -1);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int cc = c0 + j;
-      const float m = ex2_approx((Gr - s_G[cc]) * kLog2e);
-      const float rowf = isP ? p.scale * s_rq[r] : s_beta[r] * s_rk[r];
-      x[j] = (cc <= lim && r < L) ? rowf * m * s_rk[cc] * x[j] : 0.f;
-    }
+    if (p.prologue) mask_row32<true>(x, s_G, s_rk, c0, s_G[r], rowf, lim, r < L);
+    else mask_row32<false>(x, s_G, nullptr, c0, s_G[r], rowf, lim, r < L);
     if (isP) {  // q4 = 2, 3: lanes hold P rows r = R - 64; the record holds P^T
       store_transposed(ws.P(slot, hv, p.Hv), x, r, c0, 1.f, true,
                        [](int rr, int cc) { return swz<kC>(rr, cc); });

@@ -214,4 +214,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// The decay masks of one gram row (the 32 columns c0..c0+31 one thread holds): column
+// c becomes rowf * 2^(Gr - G2[c]) * colf[c] * x, kept on and left of column lim and
+// zero elsewhere and in rows past the sequence end (row_in false).  G2 is the chunk's
+// cumulative gate in log2 units (so the exponent needs no scaling), read as float4
+// (G2 + c0 16-byte aligned); COLF: multiply by colf too (the fused prologue's 1/|k|
+// per column).
+template <bool COLF>
+__device__ __forceinline__ void mask_row32(float (&x)[32], const float* G2, const float* colf,
+                                           int c0, float Gr, float rowf, int lim, bool row_in) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {  // four columns at a time: few registers live
+    const float4 v = reinterpret_cast<const float4*>(G2 + c0)[q];
+    const float g[4] = {v.x, v.y, v.z, v.w};
+    float f[4] = {1.f, 1.f, 1.f, 1.f};
+    if (COLF) {
+      const float4 w = reinterpret_cast<const float4*>(colf + c0)[q];
+      f[0] = w.x; f[1] = w.y; f[2] = w.z; f[3] = w.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = 4 * q + e;
+      const float m = ex2_approx(Gr - g[e]);
+      x[j] = (c0 + j <= lim && row_in) ? rowf * (COLF ? m * f[e] : m) * x[j] : 0.f;
+    }
+  }
+}
+
 }  // namespace gdn
