@@ -249,3 +249,41 @@ def test_many_heads_take_the_32_column_chain_tile(cuda_lib, dk, dv):
     x = make_inputs(w, device="cuda")
     o, hT = run(cuda_lib, x)
     check_heads(x, o, hT, heads=[0, 17, 39], dtype="bf16")
+
+
+@pytest.mark.parametrize("dtype,tc", [("bf16", False), ("bf16", True), ("f32", None)])
+def test_cuda_graph_replay_matches_eager(cuda_lib, dtype, tc):
+    """The prep and chain launches (the chain a programmatic dependent of the prep) and
+    a decode step captured in one CUDA graph: replaying it gives bit for bit what the
+    same calls give eagerly, and the state passes from the forward to the step."""
+    lap = cuda_lib
+    w = small(200, Hqk=2, Hv=4, dtype=dtype, seed=11)
+    x = make_inputs(w, device="cuda")
+    kw = {} if tc is None else {"tc_chain": tc}
+    tok = {n: x[n][:, 199] for n in ("q", "k", "v", "g", "beta")}
+
+    def calls(o, hT, o1):
+        lap.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], o, hT,
+                          chunk=64, scale=w.scale, **kw)
+        lap.gdn_recurrent_step(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"], hT, o1,
+                               scale=w.scale)
+
+    o_e, h_e = torch.empty_like(x["v"]), torch.empty_like(x["h0"])
+    o1_e = torch.empty_like(tok["v"])
+    calls(o_e, h_e, o1_e)
+    torch.cuda.synchronize()
+    o_g, h_g = torch.empty_like(o_e), torch.empty_like(h_e)
+    o1_g = torch.empty_like(o1_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls(o_g, h_g, o1_g)  # warm-up on the capture stream (workspace pools)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(o_g, h_g, o1_g)
+    for _ in range(3):
+        o_g.zero_(), h_g.zero_(), o1_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o_e) and torch.equal(h_g, h_e) and torch.equal(o1_g, o1_e)
