@@ -1,4 +1,4 @@
-// gdn_prep.cu - the chunk-parallel Map phase of the chunkwise forward.
+// gdn_prep_tc.cu - the chunk-parallel Map phase for the tensor-memory chain (lookahead records).
 //
 // "Empowering Hybrid Attention Models on NPUs", §2.1, Figure 1(b): operators
 // #1-#4 (Gate, KKT, Solve, W/U) depend only on one chunk's q, k, v, g, beta,
